@@ -1,0 +1,407 @@
+"""Benchmark of the causal bifocal-RoPE attention path on one B300 (or N replicas).
+
+One step = the whole hot path over one batch of synthetic input:
+  * prefill of the 4x-extension workload (L = 131072, G = 4, 32 query / 8 KV
+    heads, d = 128, w0 = 4096, theta = 1e6): RoPE stage + routed attention;
+  * decode against one absolute-position cache at L = 32767, 32769, 65537,
+    131072 (G = 1, 2, 3, 4), one new token each.
+
+`value` is the prefill throughput in TFLOP/s of causal-pair FLOPs (4 * d per
+pair per query head), RoPE stage included; decode is reported beside it in
+HBM GB/s and tokens/s.  Inputs (1.5 GB per prefill, 0.5 GB of cache) are
+larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bifocal_rope_extension_causal_b300 import synth  # noqa: E402
+from bifocal_rope_extension_causal_b300 import workloads as W  # noqa: E402
+
+METRIC = "bifocal prefill TFLOP/s & % bf16 tensor peak at 128K; decode HBM GB/s"
+PREFILL = W.EXT_128K
+DECODE = W.DECODE
+KERNELS_PER_PREFILL = 3   # RoPE (Q), RoPE (K), attention
+KERNELS_PER_DECODE = 2    # split-K partials, merge
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags)
+                          if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
+    return rank, local, world
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample(n_rows: int = 128, head: int = 0):
+    """Time the fp64 oracle on `n_rows` seeded rows of one query head of the
+    128K prefill; returns (tflops, seconds, pairs, cores)."""
+    import numpy as np
+    import oracle
+    w = PREFILL
+    if head not in _ORACLE_INPUTS:
+        q, k, v = synth.prefill_inputs(w.L, w.Hq, w.Hkv, w.d, w.index)
+        hk = head // (w.Hq // w.Hkv)
+        _ORACLE_INPUTS[head] = (q[:, :, head:head + 1].float().numpy(),
+                                k[:, :, hk:hk + 1].float().numpy(),
+                                v[:, :, hk:hk + 1].float().numpy())
+    qn, kn, vn = _ORACLE_INPUTS[head]
+    rows = np.sort(np.random.default_rng(99).choice(w.L, size=n_rows, replace=False))[None]
+    t0 = time.perf_counter()
+    oracle.bifocal_prefill(qn, kn, vn, w.w0, w.w_pretrained, w.theta, round_rotated_qk=True, rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = int((rows + 1).sum())
+    return 4.0 * w.d * pairs / dt / 1e12, dt, pairs, _cores()
+
+
+def _cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, _, world = int(os.environ.get("RANK", "0")), 0, int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(32)
+    secs, pairs = 0.0, 0
+    for _ in range(args.steps):
+        v, dt, pr, cores = oracle_sample(32)
+        vals.append(v)
+        secs += dt
+        pairs += pr
+    value = 4.0 * PREFILL.d * pairs / secs / 1e12
+    sample = (f"fp64 oracle, 4x-extension prefill (L=131072, G=4): 32 seeded query rows of head 0 "
+              f"per step ({pairs // max(args.steps, 1)} causal pairs), RoPE tables included")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict():
+    w, dw = PREFILL, DECODE
+    return {"workload": f"{w.name} + {dw.name}", "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv,
+            "d": w.d, "w0": w.w0, "w_pretrained": w.w_pretrained, "rope_theta": w.theta,
+            "decode_lengths": list(dw.lengths), "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    rank, local, world = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    import ctypes
+    import bifocal_rope_extension_causal_b300 as jl
+    from bifocal_rope_extension_causal_b300 import _capi
+    lib = _capi.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    w, dw = PREFILL, DECODE
+
+    q, k, v = synth.prefill_inputs(w.L, w.Hq, w.Hkv, w.d, w.index)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    ws_bytes = jl.prefill_workspace_size(w.B, w.L, w.Hq, w.Hkv, w.d, w.w_pretrained)
+    ws = jl.alloc_workspace(ws_bytes, dev)
+    kc, vc, qs = synth.decode_inputs(dw.Lcap, dw.Hq, dw.Hkv, dw.d, dw.index, len(dw.lengths))
+    kc, vc, qs = kc.to(dev), vc.to(dev), qs.to(dev)
+    od = torch.empty((dw.B, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
+    lsed = torch.empty((dw.B, dw.Hq), dtype=torch.float32, device=dev)
+    dws_bytes = jl.decode_workspace_size(dw.B, dw.Hq, dw.d, dw.Lcap)
+    dws = jl.alloc_workspace(dws_bytes, dev)
+    P = ctypes.c_void_p
+
+    def rope():
+        _capi.check(lib.jl_bifocal_rope(P(qd.data_ptr()), P(kd.data_ptr()), w.B, w.L, w.Hq, w.Hkv,
+                                        w.d, w.w_pretrained, w.theta, None, P(ws.data_ptr()),
+                                        ws_bytes, sp))
+
+    def attention():
+        _capi.check(lib.jl_bifocal_attention(P(vd.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()),
+                                             w.B, w.L, w.Hq, w.Hkv, w.d, w.w0, w.w_pretrained, 0.0,
+                                             P(ws.data_ptr()), ws_bytes, sp))
+
+    def decode(i, L):
+        _capi.check(lib.jl_bifocal_decode(P(qs[i].data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
+                                          L, dw.Lcap, P(od.data_ptr()), P(lsed.data_ptr()), dw.B,
+                                          dw.Hq, dw.Hkv, dw.d, dw.w0, dw.w_pretrained, dw.theta,
+                                          0.0, P(dws.data_ptr()), dws_bytes, sp))
+
+    nL = len(dw.lengths)
+
+    def step(ev):
+        ev[0].record(stream)
+        rope()
+        ev[1].record(stream)
+        attention()
+        ev[2].record(stream)
+        for i, L in enumerate(dw.lengths):
+            decode(i, L)
+            ev[3 + i].record(stream)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3 + nL)])
+    torch.cuda.synchronize()
+    jl.device_status()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3 + nL)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for s in range(args.steps):
+            step(events[s])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    jl.device_status()
+    total_ms = start.elapsed_time(stop)
+    rope_ms = [e[0].elapsed_time(e[1]) for e in events]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in events]
+    dec_us = [[1e3 * e[2 + i].elapsed_time(e[3 + i]) for e in events] for i in range(nL)]
+
+    flops = W.prefill_flops(w)
+    prefill_ms = statistics.mean(r + a for r, a in zip(rope_ms, attn_ms))
+    prefill_ms_max = max_over_ranks(prefill_ms, world)
+    total_ms = max_over_ranks(total_ms, world)
+    value = world * flops / (prefill_ms_max * 1e-3) / 1e12
+    attn_mean = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean * 1e-3) / 1e12
+    peaks, peak_src = measured_peaks()
+    peak_tf = float(peaks.get("bf16_tflops", 1800.0))
+    hbm = float(peaks.get("hbm_gbs", 6400.0))
+
+    dec = {"lengths": list(dw.lengths), "G": [jl.group_size(L, dw.w_pretrained) for L in dw.lengths],
+           "us": [], "gbs": [], "tokens_per_s": [], "frac_of_measured_hbm": [],
+           "frac_of_8tbs": [], "bytes": []}
+    for i, L in enumerate(dw.lengths):
+        us = statistics.median(dec_us[i])
+        nbytes = W.decode_bytes(L, dw.Hkv, dw.d, dw.Hq, dw.B)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        dec["us"].append(round(us, 2))
+        dec["gbs"].append(round(gbs, 1))
+        dec["bytes"].append(nbytes)
+        dec["tokens_per_s"].append(round(dw.B / (us * 1e-6), 1))
+        dec["frac_of_measured_hbm"].append(round(gbs / hbm, 4))
+        dec["frac_of_8tbs"].append(round(gbs / 8000.0, 4))
+
+    e2e = run_e2e(jl, q, k, v, w, dev, min(args.steps, 3), world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, dt, pairs, cores = oracle_sample(128)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle, 4x-extension prefill: 128 seeded query rows of head 0 "
+                         f"({pairs} causal pairs) in {dt:.1f} s, RoPE tables included"}
+    traffic = load_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)", "config": config_dict(),
+        "pct_bf16_peak": round(value / world / peak_tf, 4),
+        "prefill_ms": round(prefill_ms, 3), "rope_ms": round(statistics.mean(rope_ms), 3),
+        "attention_ms": round(attn_mean, 3),
+        "decode": dec,
+        "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": round(achieved, 1),
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (KERNELS_PER_PREFILL + nL * KERNELS_PER_DECODE),
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(jl, q, k, v, w, dev, steps, world):
+    """Same metric through the public call with host buffers: pinned q, k, v
+    copied in and o, lse copied out inside the timed region."""
+    import torch
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32).pin_memory()
+    ws = jl.alloc_workspace(jl.prefill_workspace_size(w.B, w.L, w.Hq, w.Hkv, w.d, w.w_pretrained), dev)
+    stream = torch.cuda.current_stream()
+
+    def once():
+        qd = qh.to(dev, non_blocking=True)
+        kd = kh.to(dev, non_blocking=True)
+        vd = vh.to(dev, non_blocking=True)
+        o, lse = jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    once()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        once()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": world * W.prefill_flops(w) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
+
+
+def load_traffic():
+    """DRAM bytes per attention launch from the committed ncu capture, if it
+    was taken on the current kernel (profiles/prefill_attention_traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "prefill_attention_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bytes_per_full_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

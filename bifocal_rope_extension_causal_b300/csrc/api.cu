@@ -1,0 +1,238 @@
+// C ABI of libjetlong.so (declared in include/jetlong.h): argument
+// validation, workspace carving, and the launches of the CUDA path.  The
+// library allocates no device memory; every buffer is the caller's.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+
+#include "../../include/jetlong.h"
+#include "internal.h"
+#include "positions.cuh"
+
+namespace jl {
+
+__device__ int g_device_status = 0;
+
+int* device_status_ptr() {
+  int* ptr = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_device_status) != cudaSuccess) return nullptr;
+  return ptr;
+}
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(JL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float resolve_scale(float s, int d) { return s > 0.f ? s : 1.0f / sqrtf(static_cast<float>(d)); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+RopeFreqs make_rope_freqs(int d, double theta) {
+  RopeFreqs f{};
+  for (int i = 0; i < d / 2 && i < kMaxHalfDim; ++i) f.w[i] = pow(theta, -2.0 * i / d);
+  return f;
+}
+
+}  // namespace jl
+
+using namespace jl;
+
+extern "C" {
+
+int64_t jl_group_size(int64_t L, int64_t w_pretrained) {
+  if (L < 0 || w_pretrained <= 0) return -1;
+  return jl::group_size(L, w_pretrained);
+}
+
+size_t jl_bifocal_prefill_workspace_size(int B, int L, int Hq, int Hkv, int d, int w_pretrained) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || d < 1 || w_pretrained < 1) return 0;
+  const bool bif = jl::group_size(L, w_pretrained) > 1;
+  const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * L * d * 2);
+  const size_t kbytes = align_up(static_cast<size_t>(B) * Hkv * L * d * 2);
+  return (bif ? 2 : 1) * (qbytes + kbytes);
+}
+
+namespace {
+
+// Shared validation of the prefill-family arguments; 0 if fine.
+int check_prefill_shape(const char* who, int B, int L, int Hq, int Hkv, int d, int w0,
+                        int w_pretrained) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1)
+    return fail(JL_ERR_INVALID, "%s: need B, L, Hq, Hkv >= 1 (got %d, %d, %d, %d)", who, B, L, Hq, Hkv);
+  if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "%s: Hq %% Hkv != 0 (%d, %d)", who, Hq, Hkv);
+  if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "%s: need w0 >= 0, w_pretrained >= 1", who);
+  if (d != 64 && d != 128) return fail(JL_ERR_UNSUPPORTED, "%s: head dim %d (supported: 64, 128)", who, d);
+  return JL_OK;
+}
+
+int check_workspace(const char* who, const void* ws, size_t bytes, size_t need) {
+  if (!ws || bytes < need || (reinterpret_cast<uintptr_t>(ws) % kAlign))
+    return fail(JL_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-byte aligned (got %zu)", who, need,
+                bytes);
+  return JL_OK;
+}
+
+// Workspace carving: Q_abs, K_abs, then (G > 1) Q_rem, K_rem.
+struct PrefillWs {
+  unsigned char *qa, *ka, *qr, *kr;
+};
+PrefillWs carve(const void* workspace, int B, int L, int Hq, int Hkv, int d, bool bif) {
+  auto* ws = static_cast<unsigned char*>(const_cast<void*>(workspace));
+  const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * L * d * 2);
+  const size_t kbytes = align_up(static_cast<size_t>(B) * Hkv * L * d * 2);
+  PrefillWs w;
+  w.qa = ws;
+  w.ka = ws + qbytes;
+  w.qr = bif ? ws + qbytes + kbytes : w.qa;
+  w.kr = bif ? ws + 2 * qbytes + kbytes : w.ka;
+  return w;
+}
+
+}  // namespace
+
+int jl_bifocal_rope(const void* q, const void* k, int B, int L, int Hq, int Hkv, int d,
+                    int w_pretrained, double rope_theta, void* k_rot_out, void* workspace,
+                    size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q || !k) return fail(JL_ERR_INVALID, "rope: null q/k pointer");
+  int rc = check_prefill_shape("rope", B, L, Hq, Hkv, d, 0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "rope: rope_theta must be > 0");
+  if (!aligned16(q) || !aligned16(k) || (k_rot_out && !aligned16(k_rot_out)))
+    return fail(JL_ERR_INVALID, "rope: every pointer must be 16-byte aligned");
+  rc = check_workspace("rope", workspace, workspace_bytes,
+                       jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained));
+  if (rc != JL_OK) return rc;
+  const int G = static_cast<int>(jl::group_size(L, w_pretrained));
+  const bool bif = G > 1;
+  const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, bif);
+  auto stream = static_cast<cudaStream_t>(cuda_stream);
+  const RopeFreqs fr = make_rope_freqs(d, rope_theta);
+  cudaError_t e = launch_rope_prepass(q, B, L, Hq, d, G, fr, w.qa, bif ? w.qr : nullptr, nullptr, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (Q)");
+  e = launch_rope_prepass(k, B, L, Hkv, d, G, fr, w.ka, bif ? w.kr : nullptr, k_rot_out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (K)");
+  return JL_OK;
+}
+
+int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d,
+                         int w0, int w_pretrained, float softmax_scale, const void* workspace,
+                         size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!v || !o) return fail(JL_ERR_INVALID, "attention: null v/o pointer");
+  int rc = check_prefill_shape("attention", B, L, Hq, Hkv, d, w0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return fail(JL_ERR_INVALID, "attention: every pointer must be 16-byte aligned");
+  rc = check_workspace("attention", workspace, workspace_bytes,
+                       jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained));
+  if (rc != JL_OK) return rc;
+  const int G = static_cast<int>(jl::group_size(L, w_pretrained));
+  const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, G > 1);
+  PrefillArgs a;
+  a.qa = w.qa; a.qr = w.qr; a.ka = w.ka; a.kr = w.kr; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.L = L; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
+  a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+  const cudaError_t e = launch_prefill_attention(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention: kernel launch");
+  return JL_OK;
+}
+
+int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int L, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta,
+                       float softmax_scale, void* k_rot_out, void* workspace,
+                       size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q || !k || !v || !o) return fail(JL_ERR_INVALID, "prefill: null q/k/v/o pointer");
+  int rc = check_prefill_shape("prefill", B, L, Hq, Hkv, d, w0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return fail(JL_ERR_INVALID, "prefill: every pointer must be 16-byte aligned");
+  rc = jl_bifocal_rope(q, k, B, L, Hq, Hkv, d, w_pretrained, rope_theta, k_rot_out, workspace,
+                       workspace_bytes, cuda_stream);
+  if (rc != JL_OK) return rc;
+  return jl_bifocal_attention(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, softmax_scale,
+                              workspace, workspace_bytes, cuda_stream);
+}
+
+size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap) {
+  if (B < 1 || Hq < 1 || d < 1 || Lcap < 1) return 0;
+  return align_up(decode_workspace_bytes(B, Hq, d, Lcap));
+}
+
+int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
+                      void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                      double rope_theta, float softmax_scale, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q || !k_cache || !v_cache || !o) return fail(JL_ERR_INVALID, "decode: null q/cache/o pointer");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1)
+    return fail(JL_ERR_INVALID, "decode: need B, Hq, Hkv, Lcap >= 1");
+  if (L < 1 || L > Lcap) return fail(JL_ERR_INVALID, "decode: need 1 <= L <= Lcap (got L=%d, Lcap=%d)", L, Lcap);
+  if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "decode: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
+  if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "decode: need w0 >= 0, w_pretrained >= 1");
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "decode: rope_theta must be > 0");
+  if (d != 128) return fail(JL_ERR_UNSUPPORTED, "decode: head dim %d (supported: 128)", d);
+  const int GQ = Hq / Hkv;
+  if (Hkv > 8 || (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8))
+    return fail(JL_ERR_UNSUPPORTED, "decode: need Hkv <= 8 and Hq/Hkv in {1,2,4,8} (got %d, %d)", Hkv, GQ);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return fail(JL_ERR_INVALID, "decode: every pointer must be 16-byte aligned");
+  const size_t need = jl_bifocal_decode_workspace_size(B, Hq, d, Lcap);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+    return fail(JL_ERR_WORKSPACE, "decode: workspace needs %zu bytes, 256-byte aligned (got %zu)", need,
+                workspace_bytes);
+  DecodeArgs a;
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.o = o; a.lse = lse;
+  a.part = static_cast<float*>(workspace);
+  a.B = B; a.L = L; a.Lcap = Lcap; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0;
+  a.G = static_cast<int>(jl::group_size(L, w_pretrained));
+  a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+  a.freqs = make_rope_freqs(d, rope_theta);
+  const cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
+  return JL_OK;
+}
+
+int jl_device_status(void* cuda_stream) {
+  t_err[0] = '\0';
+  auto stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status: stream sync");
+  int h = 0;
+  e = cudaMemcpyFromSymbol(&h, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "status: read");
+  if (h != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "status: clear");
+    return fail(JL_ERR_TIMEOUT, "a bounded device wait ran out (code %d)", h);
+  }
+  return JL_OK;
+}
+
+const char* jl_last_error(void) { return t_err; }
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+/*
+ * jetlong.h -- C ABI of libjetlong.so: causal bifocal-RoPE attention
+ * (dynamic bifocal RoPE, "Jet-Long: Efficient Long-Context Extension with
+ * Dynamic Bifocal RoPE") on one NVIDIA B300 (sm_103a).
+ *
+ * What the library computes.  For a query at position q and a key at
+ * position k <= q (0-based positions, causal):
+ *
+ *   local  (q - k <= w0):  S(q,k) = <R_q x_q,       R_k x_k>
+ *   remote (q - k >  w0):  S(q,k) = <R_f(q) x_q,    R_f(k) x_k>
+ *
+ * with f(x) = floor(x / G) and G = max(1, ceil(L / w_pretrained))
+ * (paper digest page, section "Method": bifocal score Eq. 1, dynamic group
+ * size and alias map Eqs. 2-3).  R_p is rotate-half RoPE: coordinate pair
+ * (x_i, x_{i+d/2}) is turned by the angle p * theta^(-2i/d) (RoFormer).
+ * The output is softmax(scale * S) V over keys k <= q, and the per-row
+ * natural-log log-sum-exp lse = log sum_k exp(scale * S(q,k)).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are CALLER-OWNED device pointers (cudaMalloc / torch); the
+ *    library allocates no device memory.  bf16 is IEEE bfloat16, fp32 is
+ *    IEEE float.  Every tensor is dense row-major in the layout stated.
+ *  - Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  A return of JL_OK means the work was
+ *    launched; device-side faults surface at the caller's next sync.
+ *  - On error nothing is launched and a message is available from
+ *    jl_last_error() (thread-local, valid until the next call).
+ *  - No CPU fallback: without a CUDA device every compute call returns
+ *    JL_ERR_CUDA.
+ */
+#ifndef JETLONG_H_
+#define JETLONG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define JL_OK               0
+#define JL_ERR_INVALID     -1  /* bad argument: null pointer, negative size, ...   */
+#define JL_ERR_UNSUPPORTED -2  /* legal but not implemented (head dim, group, ...) */
+#define JL_ERR_CUDA        -3  /* a CUDA runtime call or launch failed             */
+#define JL_ERR_TIMEOUT     -4  /* a bounded device-side wait ran out (see status)  */
+#define JL_ERR_WORKSPACE   -5  /* workspace pointer null or workspace_bytes small  */
+
+/*
+ * Dynamic group size G = max(1, ceil(L / w_pretrained))  (digest page,
+ * "Method", Eq. 2): the smallest integer g >= 1 with floor((L-1)/g) <
+ * w_pretrained, so every aliased position lies in the pretrained window.
+ * Pure host function, no device work.  Returns G >= 1 (L == 0 gives 1),
+ * or -1 if L < 0 or w_pretrained <= 0.
+ */
+int64_t jl_group_size(int64_t L, int64_t w_pretrained);
+
+/*
+ * Bytes of device workspace jl_bifocal_prefill needs for these sizes
+ * (rotated copies of Q and K at absolute and aliased positions; the
+ * aliased copies are omitted when G == 1).  Returns 0 for invalid sizes.
+ */
+size_t jl_bifocal_prefill_workspace_size(int B, int L, int Hq, int Hkv, int d,
+                                         int w_pretrained);
+
+/*
+ * Causal bifocal-RoPE attention over a whole prompt (prefill), one G for
+ * the whole call, G = jl_group_size(L, w_pretrained).
+ *
+ *  q     bf16 [B, L, Hq,  d]  raw (pre-RoPE) queries
+ *  k     bf16 [B, L, Hkv, d]  raw (pre-RoPE) keys
+ *  v     bf16 [B, L, Hkv, d]  values
+ *  o     bf16 [B, L, Hq,  d]  output (written)
+ *  lse   fp32 [B, Hq, L]      natural-log LSE of the scaled scores; may be NULL
+ *  d     head dim, 64 or 128; Hq % Hkv == 0 (query head h reads KV head
+ *        h / (Hq / Hkv)); B, L, Hq, Hkv >= 1
+ *  w0    local window (>= 0): q - k <= w0 scores at absolute positions
+ *  w_pretrained  pretrained context length (>= 1)
+ *  rope_theta    RoPE base (> 0)
+ *  softmax_scale <= 0 selects 1/sqrt(d)
+ *  k_rot_out     NULL, or bf16 [B, L, Hkv, d] receiving R_k x_k (keys rotated
+ *                at their absolute position), the form a KV cache stores
+ *                for jl_bifocal_decode
+ *  workspace     device buffer of >= jl_bifocal_prefill_workspace_size bytes,
+ *                256-byte aligned; contents on entry are ignored
+ *
+ * Inputs are read-only; o, lse, k_rot_out and the workspace are written.
+ * Buffers must not overlap.  Every pointer must be 16-byte aligned.
+ */
+int jl_bifocal_prefill(const void* q, const void* k, const void* v,
+                       void* o, float* lse,
+                       int B, int L, int Hq, int Hkv, int d,
+                       int w0, int w_pretrained, double rope_theta,
+                       float softmax_scale, void* k_rot_out,
+                       void* workspace, size_t workspace_bytes,
+                       void* cuda_stream);
+
+/*
+ * The two stages of jl_bifocal_prefill, callable separately (same arguments,
+ * same workspace).  jl_bifocal_rope rotates q and k at absolute and aliased
+ * positions into the workspace (and writes k_rot_out if not NULL);
+ * jl_bifocal_attention then runs the routed causal attention over the
+ * workspace and v.  Calling both in order on one stream is exactly
+ * jl_bifocal_prefill.  jl_bifocal_attention reads nothing but the workspace
+ * written by a jl_bifocal_rope call with the same B, L, Hq, Hkv, d and
+ * w_pretrained.
+ */
+int jl_bifocal_rope(const void* q, const void* k,
+                    int B, int L, int Hq, int Hkv, int d,
+                    int w_pretrained, double rope_theta, void* k_rot_out,
+                    void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+int jl_bifocal_attention(const void* v, void* o, float* lse,
+                         int B, int L, int Hq, int Hkv, int d,
+                         int w0, int w_pretrained, float softmax_scale,
+                         const void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
+
+/*
+ * Bytes of device workspace jl_bifocal_decode needs (per-split partial
+ * softmax statistics and outputs) for caches of up to Lcap positions.
+ * Returns 0 for invalid sizes.
+ */
+size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap);
+
+/*
+ * One new query token against an absolute-position KV cache (decode), with
+ * the on-the-fly correction rotation of the digest page's "KV cache
+ * invariant" (Delta_q = f(q) - q, Delta_k = f(k) - k, R_a R_b = R_{a+b}):
+ * the cache is read, never rewritten, whatever G is.
+ *
+ *  q        bf16 [B, Hq, d]          raw (pre-RoPE) query of the token at
+ *                                    position L-1
+ *  k_cache  bf16 [B, Lcap, Hkv, d]   key j holds R_j x_j (rotated at its
+ *                                    absolute position j); read-only
+ *  v_cache  bf16 [B, Lcap, Hkv, d]   values; read-only
+ *  L        number of valid cache positions INCLUDING the new token
+ *           (1 <= L <= Lcap); G = jl_group_size(L, w_pretrained)
+ *  o        bf16 [B, Hq, d]   output
+ *  lse      fp32 [B, Hq]      natural-log LSE; may be NULL
+ *  d        128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}; Hkv <= 8
+ *  workspace >= jl_bifocal_decode_workspace_size(B, Hq, d, Lcap) bytes
+ *
+ *   local  (L-1 - j <= w0):  s_j = <R_{L-1} x_q, K_j>
+ *   remote (L-1 - j >  w0):  s_j = <R_{f(L-1)} x_q, R_{f(j)-j} K_j>
+ */
+int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache,
+                      int L, int Lcap, void* o, float* lse,
+                      int B, int Hq, int Hkv, int d,
+                      int w0, int w_pretrained, double rope_theta,
+                      float softmax_scale,
+                      void* workspace, size_t workspace_bytes,
+                      void* cuda_stream);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the library's device
+ * status word, which a kernel sets when one of its bounded waits on a
+ * barrier runs out (it then skips its remaining work instead of hanging).
+ * Returns JL_OK, JL_ERR_TIMEOUT (message in jl_last_error) or JL_ERR_CUDA.
+ */
+int jl_device_status(void* cuda_stream);
+
+/* Message of the last error on this thread ("" if none). Never NULL. */
+const char* jl_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JETLONG_H_ */

@@ -1,0 +1,83 @@
+"""Decode parity: the CUDA split-K decode (through the C ABI) against the fp64
+oracle, on the whole key range.  The cache is checksummed before and after
+every step: it is read, never rewritten, while G crosses 1 -> 2 -> 3 -> 4."""
+
+import numpy as np
+import pytest
+
+import oracle
+from bifocal_rope_extension_causal_b300 import synth, workloads as W
+from gpu_common import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jl():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import bifocal_rope_extension_causal_b300 as mod
+    from bifocal_rope_extension_causal_b300 import build
+    build.build()
+    return mod
+
+
+def check_decode(jl, kc, vc, q, L, w0, wp, theta, tag):
+    o, lse = jl.decode(q.cuda() if not q.is_cuda else q, kc, vc, L, w0, wp, theta)
+    jl.device_status()
+    o_ref, l_ref = oracle.bifocal_decode(q.float().cpu().numpy(), kc[:, :L].float().cpu().numpy(),
+                                         vc[:, :L].float().cpu().numpy(), L, w0, wp, theta)
+    return assert_close(to_np(o), to_np(lse), o_ref, l_ref, tag)
+
+
+def test_decode_workload_cache_invariant(jl):
+    """The decode workload: one cache, lengths 32767, 32769, 65537, 131072
+    (G = 1, 2, 3, 4), the cache bytes unchanged after every step."""
+    import torch
+    w = W.DECODE
+    kc, vc, qs = synth.decode_inputs(w.Lcap, w.Hq, w.Hkv, w.d, w.index, len(w.lengths))
+    kc, vc = kc.cuda(), vc.cuda()
+    sums = (kc.view(torch.int16).long().sum().item(), vc.view(torch.int16).long().sum().item())
+    for step, L in enumerate(w.lengths):
+        G = jl.group_size(L, w.w_pretrained)
+        assert G == step + 1
+        check_decode(jl, kc, vc, qs[step], L, w.w0, w.w_pretrained, w.theta, f"decode L={L} G={G}")
+        now = (kc.view(torch.int16).long().sum().item(), vc.view(torch.int16).long().sum().item())
+        assert now == sums, "the KV cache was modified"
+
+
+@pytest.mark.parametrize("L,Lcap,Hq,Hkv,wp,w0", [
+    (1, 8, 4, 2, 4, 0),          # only the new token
+    (2, 2, 4, 4, 1, 0),          # G = 2, w0 = 0
+    (7, 40, 8, 1, 3, 2),         # ragged, G = 3, 8 query heads per KV head
+    (64, 64, 2, 2, 16, 5),       # exactly one 64-key block
+    (65, 100, 4, 1, 16, 0),      # one key past a block
+    (300, 300, 16, 8, 40, 17),   # G = 8, local/remote boundary inside a warp step
+    (1000, 1200, 32, 8, 300, 64),
+    (1000, 1000, 8, 8, 2000, 10),  # G = 1
+    (777, 800, 4, 2, 100, 776),  # w0 >= L-1: all local at G = 8
+])
+def test_decode_small(jl, L, Lcap, Hq, Hkv, wp, w0):
+    kc, vc, qs = synth.decode_inputs(Lcap, Hq, Hkv, 128, L + 3 * w0, 1)
+    check_decode(jl, kc.cuda(), vc.cuda(), qs[0], L, w0, wp, 1e4, f"L={L} Hq={Hq} Hkv={Hkv}")
+
+
+def test_decode_batch(jl):
+    kc, vc, qs = synth.decode_inputs(500, 8, 2, 128, 9, 1, B=3)
+    check_decode(jl, kc.cuda(), vc.cuda(), qs[0], 450, 30, 100, 1e6, "B=3")
+
+
+def test_decode_matches_prefill_rows(jl):
+    """Prefill fills the cache (k_rot_out); decode at length L' then agrees
+    with prefill row L'-1 when both see the same G (here L' > w_p * (G-1))."""
+    import torch
+    L, Hq, Hkv, d, wp, w0 = 700, 8, 2, 128, 200, 50
+    q, k, v = synth.prefill_inputs(L, Hq, Hkv, d, 21)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    krot = torch.empty_like(kd)
+    o_pre, lse_pre = jl.prefill(qd, kd, vd, w0, wp, 1e4, k_rot_out=krot)
+    for Lp in (601, 650, 700):  # G(Lp) == G(700) == 4
+        o_dec, lse_dec = jl.decode(qd[:, Lp - 1].contiguous(), krot, vd, Lp, w0, wp, 1e4)
+        assert np.abs(to_np(o_dec) - to_np(o_pre[:, Lp - 1])).max() <= 3e-2, Lp
+        assert np.abs(to_np(lse_dec) - to_np(lse_pre[:, :, Lp - 1])).max() <= 2e-3, Lp
+    jl.device_status()
