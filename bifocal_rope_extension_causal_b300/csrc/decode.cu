@@ -151,9 +151,9 @@ decode_partial_kernel(DecodeKParams p) {
   for (int s = 0; s < kStages - 1; ++s) issue_step(s);
 
   // Query rotations: R_{L-1} x_q and R_{f(L-1)} x_q, times scale * log2(e).
-  if (tid < 64) {
-    s_qcs[0][tid] = rope_cos_sin(qpos, p.freqs.w[tid]);
-    s_qcs[1][tid] = rope_cos_sin(alias(qpos, p.G), p.freqs.w[tid]);
+  for (int i = tid; i < 64; i += nthr) {
+    s_qcs[0][i] = rope_cos_sin(qpos, p.freqs.w[i]);
+    s_qcs[1][i] = rope_cos_sin(alias(qpos, p.G), p.freqs.w[i]);
   }
   const bool any_remote = bifocal && js < first_local;
   if (any_remote) {
@@ -171,7 +171,7 @@ decode_partial_kernel(DecodeKParams p) {
       const float2 r = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
       s_pow[idx] = make_float2(r.x, -r.y);  // R_{-2^b}
     }
-    if (tid < 64) s_offs[tid] = make_float2(1.f, 0.f);
+    for (int i = tid; i < 64; i += nthr) s_offs[i] = make_float2(1.f, 0.f);
     __syncthreads();
     // R_{-n} = R_{-(n - 2^b)} R_{-2^b}, b = top bit of n, built layer by layer.
     for (int bb = 0; bb < 7; ++bb) {
@@ -182,7 +182,7 @@ decode_partial_kernel(DecodeKParams p) {
       }
       __syncthreads();
     }
-    if (tid < 64) s_base[tid] = rope_cos_sin(alias_offset(js, p.G), p.freqs.w[tid]);
+    for (int i = tid; i < 64; i += nthr) s_base[i] = rope_cos_sin(alias_offset(js, p.G), p.freqs.w[i]);
   }
   __syncthreads();
   const __nv_bfloat16* qin = p.q + static_cast<long long>(b) * p.Hq * kD;
@@ -215,10 +215,10 @@ decode_partial_kernel(DecodeKParams p) {
     if ((it % (kBlockKeys / kStep)) == 0 && bifocal && j0 < first_local) {
       // Rotation table of this 64-key block: cs[t] = base(j0) R_{-n(t)}.
       __syncthreads();
-      if (j0 != js && tid < 64) {
+      if (j0 != js) {
         const int jp = j0 - kBlockKeys;  // advance the base from the previous block
         const int n = alias_offset(jp, p.G) - alias_offset(j0, p.G);
-        s_base[tid] = compose(s_base[tid], s_offs[n * 64 + tid]);
+        for (int i = tid; i < 64; i += nthr) s_base[i] = compose(s_base[i], s_offs[n * 64 + i]);
       }
       __syncthreads();
       const int fj0 = alias(j0, p.G);
