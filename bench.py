@@ -377,6 +377,34 @@ def run_e2e(jl, q, k, v, w, dev, steps, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
 
 
+def run_profile_prefill(args):
+    """Small-case prefill for ncu captures: same heads, d, w0, w_pretrained and
+    theta as the 4x-extension workload, sequence length from the flag."""
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    w = PREFILL
+    L = int(args.profile_prefill)
+    dev = torch.device("cuda", 0)
+    q, k, v = synth.prefill_inputs(L, w.Hq, w.Hkv, w.d, w.index)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws = jl.alloc_workspace(jl.prefill_workspace_size(1, L, w.Hq, w.Hkv, w.d, w.w_pretrained), dev)
+    for _ in range(args.warmup):
+        jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws)
+    b.record()
+    torch.cuda.synchronize()
+    jl.device_status()
+    ms = a.elapsed_time(b) / args.steps
+    flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
+    print(json.dumps({"profile_prefill_L": L, "G": jl.group_size(L, w.w_pretrained), "ms": ms,
+                      "tflops": flops / (ms * 1e-3) / 1e12}))
+    return 0
+
+
 def load_traffic():
     """DRAM bytes per attention launch from the committed ncu capture, if it
     was taken on the current kernel (profiles/prefill_attention_traffic.json)."""
@@ -396,10 +424,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
+                    help="profiling mode: only the prefill of the 4x-extension head layout at "
+                         "sequence length L (G from L), warm-up + steps calls; prints timings")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_prefill:
+        return run_profile_prefill(args)
     return run_ours(args)
 
 

@@ -1,6 +1,7 @@
 // Launchers shared between the C-ABI layer (api.cu) and the kernel files.
 // Host-only declarations; no torch types anywhere in this library.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -53,6 +54,12 @@ struct DecodeArgs {
 int decode_max_splits();
 size_t decode_workspace_bytes(int B, int Hq, int d, int Lcap);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ---- TMA descriptors (tma_host.cu) -------------------------------------------
+// Encode a tiled bf16 tensor map: dims[0] innermost; strides_bytes[i] is the
+// byte stride of dimension i+1; box[i] the tile extent.  False on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
 
 // ---- Device status word (api.cu) ----------------------------------------------
 // Device address of the library's status word; kernels with bounded waits set

@@ -1,0 +1,460 @@
+// Causal bifocal attention over pre-rotated operands on the sm_100-family
+// tensor cores (tcgen05.mma, accumulators in tensor memory, TMA-fed
+// shared-memory ring, warp-specialised roles).
+//
+// Routing (paper digest page, "Method", Eq. 1).  A CTA owns two 128-row query
+// tiles of one head (rows q0 .. q0+255) and walks the key tiles in two
+// phases: first the "remote" visits, key tiles that hold pairs with
+// q - k > w0, scored with Q_rem K_rem^T (both rotated at aliased positions
+// f(x) = floor(x / G)); then the "local" visits, key tiles that hold pairs
+// with 0 <= q - k <= w0, scored with Q_abs K_abs^T.  A key tile that straddles
+// the q - k = w0 band is visited once in each phase, each visit masked to its
+// own pairs, so every causal pair is scored exactly once with the right
+// rotation and only straddling tiles pay for two score sets.  The online
+// softmax makes the order of visits irrelevant.  Only one rotation of Q is
+// resident at a time: after the last remote visit the Q tiles are reloaded
+// with the absolute rotation.
+//
+// Roles (10 warps):
+//   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax of query tile 1
+//   warp  8    tensor-core issue (one thread) and TMEM allocation
+//   warp  9    TMA producer (one thread)
+// Tensor memory (512 columns): S_0, S_1 (fp32 scores, 128 columns each),
+// O_0, O_1 (fp32 outputs); P_t (bf16 probabilities) overwrites the first 64
+// columns of S_t and feeds the PV product straight from tensor memory.
+// Per visit the issue order is PV(t, v-1) then QK(t, v) for t = 0, 1, so the
+// tensor core works on one tile while the softmax warps work on the other.
+//
+// Softmax: base-2 exponentials with scale * log2(e) folded in; the running
+// max is raised only when it grows by more than 8 (log2 units), so O is
+// rescaled in tensor memory rarely.  The row log-sum-exp is exported in
+// natural log.  Every barrier wait is bounded: on expiry the CTA records a
+// status code, drains its tensor-core work and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+#include "positions.cuh"
+#include "sm100.cuh"
+
+namespace jl {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;                    // rows per query tile
+constexpr int kBN = 128;                    // keys per key tile
+constexpr int kBoxBytes = 128 * 64 * 2;     // one 128-row x 64-column swizzled box
+constexpr int kSlots = 5;                   // K/V ring depth
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (~2 s)
+constexpr float kRescaleThreshold = 8.0f;       // log2 units
+
+// Per head dim D: a tile is D/64 boxes of 128 rows x 64 columns.
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kSmemBytes = 2 * kTileBytes + kSlots * kTileBytes + 1024;  // + alignment slack
+  // Matrix descriptor strides of the value tile read as an MN-major B
+  // operand: LBO = distance between 64-column boxes, SBO = 8 key rows.
+  static constexpr uint32_t kVLbo = kBoxBytes;
+  static constexpr uint32_t kVSbo = 1024;
+};
+
+struct TcParams {
+  int B, L, Hq, Hkv, w0, G, npairs;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+};
+
+// The visits of one CTA: v < nr are remote visits of key tile v; the rest
+// are local visits of key tiles jl0 .. jmax.
+struct Plan {
+  int nr, jl0, jmax, nv;
+};
+
+__device__ __forceinline__ Plan make_plan(int q0, int L, int w0) {
+  Plan p;
+  const int qlast = min(q0 + 2 * kBM - 1, L - 1);
+  p.jmax = qlast / kBN;
+  const int t = qlast - w0 - 1;  // remote pairs with key tile j iff kBN * j <= t
+  p.nr = t >= 0 ? min(t / kBN, p.jmax) + 1 : 0;
+  const int u = q0 - (kBN - 1) - w0;  // local pairs with key tile j iff kBN * j >= u
+  p.jl0 = u <= 0 ? 0 : (u + kBN - 1) / kBN;
+  p.nv = p.nr + (p.jmax - p.jl0 + 1);
+  return p;
+}
+
+__device__ __forceinline__ void visit_of(const Plan& p, int v, int& j, bool& remote) {
+  remote = v < p.nr;
+  j = remote ? v : p.jl0 + (v - p.nr);
+}
+
+struct Bars {
+  uint64_t q_full, q_empty, mma_final;
+  uint64_t full[kSlots], empty[kSlots];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_qr,
+                  const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_kr,
+                  const __grid_constant__ CUtensorMap tm_v, TcParams prm) {
+  constexpr int kTileBytes = Cfg<D>::kTileBytes;
+  constexpr int kBoxes = D / 64;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = smem_base;                  // 2 query tiles
+  const uint32_t sRing = smem_base + 2 * kTileBytes;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = prm.B * prm.Hq;
+  const int u = blockIdx.x;
+  const int pair = prm.npairs - 1 - u / BH;  // longest rows first
+  const int bh = u % BH;
+  const int b = bh / prm.Hq, h = bh % prm.Hq;
+  const int hk = h / (prm.Hq / prm.Hkv);
+  const int q0 = pair * 2 * kBM;
+  const Plan plan = make_plan(q0, prm.L, prm.w0);
+
+  auto bar = [](uint64_t& x) { return smem_u32(&x); };
+
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(bar(bars.q_full), 1);
+    mbar_init(bar(bars.q_empty), 1);
+    mbar_init(bar(bars.mma_final), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(bars.full[s]), 1);
+      mbar_init(bar(bars.empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(bars.s_full[t]), 1);
+      mbar_init(bar(bars.p_full[t]), 4 * 32);
+      mbar_init(bar(bars.pv_done[t]), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&s_tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tensormap(&tm_qa);
+    prefetch_tensormap(&tm_qr);
+    prefetch_tensormap(&tm_ka);
+    prefetch_tensormap(&tm_kr);
+    prefetch_tensormap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  auto fail = [&](int code) {
+    s_abort = 1;
+    atomicCAS(prm.status, 0, code);
+  };
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int qz = b * prm.Hq + h, kz = b * prm.Hkv + hk;
+      auto load_q = [&](const CUtensorMap* m) {
+        mbar_arrive_expect_tx(bar(bars.q_full), 2 * kTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, m, bar(bars.q_full), 64 * c, q0 + t * kBM, qz);
+      };
+      load_q(plan.nr > 0 ? &tm_qr : &tm_qa);
+      bool ok = true;
+      int idx = 0;
+      for (int v = 0; v < plan.nv && ok; ++v) {
+        int j;
+        bool remote;
+        visit_of(plan, v, j, remote);
+        if (v == plan.nr && v > 0) {  // switch the resident Q rotation
+          if (!(ok = mbar_wait(bar(bars.q_empty), 0, &s_abort, kWaitLimit))) { fail(1); break; }
+          load_q(&tm_qa);
+        }
+        for (int part = 0; part < 2 && ok; ++part, ++idx) {  // K then V
+          const int s = idx % kSlots, use = idx / kSlots;
+          if (use > 0 && !(ok = mbar_wait(bar(bars.empty[s]), (use - 1) & 1, &s_abort, kWaitLimit))) {
+            fail(2);
+            break;
+          }
+          const uint32_t dst = sRing + s * kTileBytes;
+          mbar_arrive_expect_tx(bar(bars.full[s]), kTileBytes);
+          for (int c = 0; c < kBoxes; ++c) {
+            if (part == 0)
+              tma_load_3d(dst + c * kBoxBytes, remote ? &tm_kr : &tm_ka, bar(bars.full[s]), 64 * c, j * kBN, kz);
+            else
+              tma_load_4d(dst + c * kBoxBytes, &tm_v, bar(bars.full[s]), 64 * c, hk, j * kBN, b);
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tensor-core issue
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false);
+      const uint32_t id_pv = idesc_bf16_f32(kBM, D, true);
+      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, kWaitLimit);
+      if (!ok) fail(3);
+      auto wait_slot = [&](int idx) {
+        const int s = idx % kSlots;
+        if (!mbar_wait(bar(bars.full[s]), (idx / kSlots) & 1, &s_abort, kWaitLimit)) { fail(4); return false; }
+        tc_fence_after();
+        return true;
+      };
+      auto pv = [&](int t, int vprev) {  // O_t += P_t V(vprev)
+        if (!mbar_wait(bar(bars.p_full[t]), vprev & 1, &s_abort, kWaitLimit)) { fail(5); return false; }
+        tc_fence_after();
+        const uint32_t vs = sRing + ((2 * vprev + 1) % kSlots) * kTileBytes;
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                 desc_sw128(vs + kk * 2048, Cfg<D>::kVLbo, Cfg<D>::kVSbo),
+                 id_pv, (vprev > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(bars.pv_done[t]));
+        return true;
+      };
+      for (int v = 0; v < plan.nv && ok; ++v) {
+        if (v > 0 && !(ok = wait_slot(2 * (v - 1) + 1))) break;  // V of the previous visit
+        if (!(ok = wait_slot(2 * v))) break;                     // K of this visit
+        const uint32_t ks = sRing + ((2 * v) % kSlots) * kTileBytes;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (v > 0) {
+            if (!(ok = pv(t, v - 1))) break;
+            if (t == 1) mma_commit(bar(bars.empty[(2 * (v - 1) + 1) % kSlots]));
+          }
+          if (t == 0 && v == plan.nr && v > 0) {  // first local visit: Q_abs resident?
+            if (!(ok = mbar_wait(bar(bars.q_full), 1, &s_abort, kWaitLimit))) { fail(6); break; }
+            tc_fence_after();
+          }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + t * 128, desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
+                   desc_sw128(ks + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(bars.s_full[t]));
+        }
+        if (!ok) break;
+        mma_commit(bar(bars.empty[(2 * v) % kSlots]));
+        if (v == plan.nr - 1 && plan.nr < plan.nv) mma_commit(bar(bars.q_empty));
+      }
+      if (ok) {
+        const int vl = plan.nv - 1;
+        ok = wait_slot(2 * vl + 1);
+        for (int t = 0; t < 2 && ok; ++t) ok = pv(t, vl);
+        if (ok) mma_commit(bar(bars.empty[(2 * vl + 1) % kSlots]));
+      }
+      // Drain: every MMA issued by this thread completes before TMEM is freed.
+      mma_commit(bar(bars.mma_final));
+      const volatile int never = 0;
+      if (!mbar_wait(bar(bars.mma_final), 0, &never, kWaitLimit)) atomicCAS(prm.status, 0, 7);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int t = warp >> 2;           // query tile
+    const int r = (warp & 3) * 32 + lane;  // row in tile = TMEM lane
+    const int q = q0 + t * kBM + r;
+    const int q0t = q0 + t * kBM;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * 128;  // D columns
+    const float sc = prm.scale_log2;
+    const int w0 = prm.w0;
+    float m_used = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int v = 0; v < plan.nv; ++v) {
+      int j;
+      bool remote;
+      visit_of(plan, v, j, remote);
+      const int k0 = j * kBN;
+      if (!(ok = mbar_wait(bar(bars.s_full[t]), v & 1, &s_abort, kWaitLimit))) { fail(8); break; }
+      tc_fence_after();
+      uint32_t a0[32], a1[32], a2[32], a3[32];
+      tmem_ld32(tS + 0, a0);
+      tmem_ld32(tS + 32, a1);
+      tmem_ld32(tS + 64, a2);
+      tmem_ld32(tS + 96, a3);
+      tmem_ld_wait(a0);
+      tmem_ld_wait(a1);
+      tmem_ld_wait(a2);
+      tmem_ld_wait(a3);
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(a0[i]);
+        s[32 + i] = __uint_as_float(a1[i]);
+        s[64 + i] = __uint_as_float(a2[i]);
+        s[96 + i] = __uint_as_float(a3[i]);
+      }
+      // Masks are needed only on tiles at the window band or the diagonal.
+      const bool need_mask = remote ? (q0t - (k0 + kBN - 1) <= w0)
+                                    : ((q0t + kBM - 1 - k0 > w0) || (k0 + kBN - 1 > q0t));
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int dist = q - (k0 + c);
+          const bool keep = remote ? (dist > w0) : (dist >= 0 && dist <= w0);
+          if (!keep) s[c] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_used, mx * sc);
+      float factor = 1.f;
+      if (m_new > m_used + kRescaleThreshold) {
+        factor = ex2_approx(m_used - m_new);  // 0 when m_used is -inf
+        m_used = m_new;
+      }
+      const float m_exp = (m_used == -INFINITY) ? 0.f : m_used;
+      float rowsum = 0.f;
+      uint32_t pk0[32], pk1[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2_approx(fmaf(s[2 * i], sc, -m_exp));
+        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, -m_exp));
+        rowsum += p0 + p1;
+        pk0[i] = pack_bf16x2(p0, p1);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2_approx(fmaf(s[64 + 2 * i], sc, -m_exp));
+        const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], sc, -m_exp));
+        rowsum += p0 + p1;
+        pk1[i] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * factor + rowsum;
+      tmem_st32(tS + 0, pk0);
+      tmem_st32(tS + 32, pk1);
+      // Rescale O_t in tensor memory when any row of this warp raised its max.
+      if (v > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+        if (!(ok = mbar_wait(bar(bars.pv_done[t]), (v - 1) & 1, &s_abort, kWaitLimit))) { fail(9); break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(bars.p_full[t]));
+    }
+    if (ok && mbar_wait(bar(bars.pv_done[t]), (plan.nv - 1) & 1, &s_abort, kWaitLimit)) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      __nv_bfloat16* orow = prm.o + ((static_cast<long long>(b) * prm.L + q) * prm.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait(o);
+        if (q < prm.L) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+            dst[i] = w;
+          }
+        }
+      }
+      if (q < prm.L && prm.lse != nullptr)
+        prm.lse[(static_cast<long long>(b) * prm.Hq + h) * prm.L + q] =
+            (m_used + log2f(l_run)) * 0.69314718055994531f;
+    } else if (ok) {
+      fail(10);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
+  CUtensorMap tqa, tqr, tka, tkr, tv;
+  const uint32_t box3[3] = {64, kBM, 1};
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.L),
+                              static_cast<uint64_t>(a.B) * a.Hq};
+    const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(a.L) * D * 2ull};
+    if (!make_tmap_bf16(&tqa, a.qa, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tqr, a.qr, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.L),
+                              static_cast<uint64_t>(a.B) * a.Hkv};
+    const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(a.L) * D * 2ull};
+    if (!make_tmap_bf16(&tka, a.ka, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tkr, a.kr, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv),
+                              static_cast<uint64_t>(a.L), static_cast<uint64_t>(a.B)};
+    const uint64_t strides[3] = {D * 2ull, static_cast<uint64_t>(a.Hkv) * D * 2ull,
+                                 static_cast<uint64_t>(a.L) * a.Hkv * D * 2ull};
+    const uint32_t box4[4] = {64, 1, kBN, 1};
+    if (!make_tmap_bf16(&tv, a.v, 4, dims, strides, box4, true)) return cudaErrorInvalidValue;
+  }
+  TcParams p;
+  p.B = a.B;
+  p.L = a.L;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  // One G for the call; with G == 1 both rotations coincide, so every pair
+  // is scored in the local phase (no window).
+  p.w0 = (a.G == 1 || a.w0 >= a.L) ? (1 << 30) : a.w0;
+  p.G = a.G;
+  p.npairs = (a.L + 2 * kBM - 1) / (2 * kBM);
+  p.scale_log2 = a.scale_log2;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.status = status;
+  constexpr int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = static_cast<long long>(p.npairs) * a.B * a.Hq;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prefill_tc_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(tqa, tqr, tka, tkr, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream) {
+  int* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorInvalidSymbol;
+  if (a.d == 128) return launch_tc<128>(a, status, stream);
+  if (a.d == 64) return launch_tc<64>(a, status, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace jl
