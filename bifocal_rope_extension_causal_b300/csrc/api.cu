@@ -49,6 +49,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
 
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 RopeFreqs make_rope_freqs(int d, double theta) {
   RopeFreqs f{};
   for (int i = 0; i < d / 2 && i < kMaxHalfDim; ++i) f.w[i] = pow(theta, -2.0 * i / d);

@@ -61,6 +61,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
 
+// ---- Errors (api.cu) -----------------------------------------------------------
+// Record `msg` as this thread's jl_last_error() message; returns `code`.
+int set_error(int code, const char* msg);
+
 // ---- Device status word (api.cu) ----------------------------------------------
 // Device address of the library's status word; kernels with bounded waits set
 // it (non-zero) when a wait runs out.  nullptr if it cannot be resolved.

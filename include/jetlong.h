@@ -152,6 +152,34 @@ int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache,
                       void* cuda_stream);
 
 /*
+ * jl_bifocal_decode for callers that cannot allocate device memory.  There is
+ * no counterpart on the paper's pages: this is a deployment variant.
+ *
+ * Same arguments, semantics and kernels as jl_bifocal_decode minus the
+ * workspace: the split-K partials live in a fixed 16 MiB scratch array that
+ * is part of the library image (every GPU that loads the library holds it
+ * until the process exits).  It serves B * Hq <= 63 at d = 128; larger sizes
+ * return JL_ERR_UNSUPPORTED with a message.  The entry point itself calls no
+ * allocator of any kind.
+ *  - The first call on each device (with that device current) resolves the
+ *    scratch array's device address; make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array: calls whose kernels overlap on the GPU
+ *    (other streams, unordered threads) race and corrupt each other's
+ *    results.  Order them on one stream.
+ *  - Nothing in the array needs to start at zero; each call writes every
+ *    slot it reads.
+ */
+int jl_bifocal_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                              int L, int Lcap, void* o, float* lse,
+                              int B, int Hq, int Hkv, int d,
+                              int w0, int w_pretrained, double rope_theta,
+                              float softmax_scale, void* cuda_stream);
+
+/* Size in bytes of the fixed scratch array of jl_bifocal_decode_noalloc. */
+size_t jl_bifocal_decode_noalloc_scratch_bytes(void);
+
+/*
  * Synchronises `cuda_stream`, then reads and clears the library's device
  * status word, which a kernel sets when one of its bounded waits on a
  * barrier runs out (it then skips its remaining work instead of hanging).
