@@ -405,15 +405,51 @@ def run_profile_prefill(args):
     return 0
 
 
+def run_profile_decode(args):
+    """Decode steps of the decode workload at one cache length, for ncu."""
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    dw = DECODE
+    L = int(args.profile_decode)
+    dev = torch.device("cuda", 0)
+    kc, vc, qs = synth.decode_inputs(dw.Lcap, dw.Hq, dw.Hkv, dw.d, dw.index, 1)
+    kc, vc, q = kc.to(dev), vc.to(dev), qs[0].to(dev)
+    ws = jl.alloc_workspace(jl.decode_workspace_size(dw.B, dw.Hq, dw.d, dw.Lcap), dev)
+    o = torch.empty((dw.B, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((dw.B, dw.Hq), dtype=torch.float32, device=dev)
+    run = lambda: jl.decode(q, kc, vc, L, dw.w0, dw.w_pretrained, dw.theta, out=o, lse=lse, workspace=ws)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    jl.device_status()
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    nbytes = W.decode_bytes(L, dw.Hkv, dw.d, dw.Hq, dw.B)
+    print(json.dumps({"profile_decode_L": L, "G": jl.group_size(L, dw.w_pretrained), "us": us,
+                      "gbs": nbytes / (us * 1e-6) / 1e9}))
+    return 0
+
+
 def load_traffic():
-    """DRAM bytes per attention launch from the committed ncu capture, if it
-    was taken on the current kernel (profiles/prefill_attention_traffic.json)."""
+    """DRAM bytes per attention launch from the committed ncu capture
+    (profiles/prefill_attention_traffic.json), or None if the kernel sources
+    changed since the counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "prefill_attention_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return d.get("bytes_per_full_launch")
-    except (OSError, ValueError):
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return d["bytes_per_full_launch"] if h.hexdigest() == d["sources_sha256"] else None
+    except (OSError, ValueError, KeyError):
         return None
 
 
@@ -424,6 +460,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="L",
+                    help="profiling mode: only decode steps of the decode workload at cache length L")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                     help="profiling mode: only the prefill of the 4x-extension head layout at "
                          "sequence length L (G from L), warm-up + steps calls; prints timings")
@@ -433,6 +471,8 @@ def main():
         return run_reference(args)
     if args.profile_prefill:
         return run_profile_prefill(args)
+    if args.profile_decode:
+        return run_profile_decode(args)
     return run_ours(args)
 
 

@@ -7,10 +7,11 @@
 // R_{f(j)} x_j, while the query is rotated at f(q) (Delta_q = f(q) - q).
 //
 // Work split.  The key range [0, L) is cut into `nsplit` contiguous slices
-// (whole 64-key blocks), one CTA each; a CTA covers all KV heads of its slice
-// (warp w <-> KV head w), so per-key rotation tables are built once and
-// shared by all heads.  Each CTA writes an unnormalised partial (running max
-// m, sum l, sum p v) per query head; a second kernel merges the slices with
+// (whole 64-key blocks), one CTA each, about one per SM; a CTA covers all KV
+// heads of its slice (warp w <-> KV head w), so the per-key rotation tables
+// are built once and shared by all heads.  Each CTA writes an unnormalised
+// partial (running max m, sum l, sum p v) per query head; a second kernel,
+// launched as a programmatic dependent of the first, merges the slices with
 // log-sum-exp weights.
 //
 // Memory path.  Each warp streams its head's K and V rows (256 B each per
@@ -27,8 +28,12 @@
 //
 // Lane layout.  A warp takes 8 keys per step: half-warp `half` (lane >> 4)
 // holds keys of parity `half`, lane m = lane & 15 holds head-dim elements
-// 4m..4m+3 and 64+4m..64+4m+3 (the rotate-half partners); the 16-lane
-// partial dot products are summed with a transpose-reduction.
+// 4m..4m+3 and 64+4m..64+4m+3 (the rotate-half partners).  Rotation, dot
+// products and the P V update use packed two-wide fp32 FMAs.  The 16-lane
+// partial dot products of the step's GQ x 4 (head, key) scores are summed
+// with one transpose-reduction that leaves each sum in one lane, and the
+// softmax runs once per (head, key) through a small per-warp exchange
+// buffer in shared memory.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -48,6 +53,11 @@ constexpr int kSlots = kStep / 2;
 constexpr int kStages = 3;      // per-warp ring depth
 constexpr int kMaxSplits = 512;
 constexpr int kStageBytes = kStep * 2 * kD * 2;  // K and V rows of one step
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+
+// Per-warp exchange buffer (z[GQ][8], p[8][GQ], alpha[GQ]) in floats, padded
+// to 16 bytes so that the cp.async ring after it stays 16-byte aligned.
+__host__ __device__ constexpr int exchange_floats(int gq) { return (17 * gq + 3) / 4 * 4; }
 
 struct DecodeKParams {
   const __nv_bfloat16* q;
@@ -70,44 +80,63 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-__device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
-  f[0] = __uint_as_float(u.x << 16);
-  f[1] = __uint_as_float(u.x & 0xffff0000u);
-  f[2] = __uint_as_float(u.y << 16);
-  f[3] = __uint_as_float(u.y & 0xffff0000u);
+// Four bf16 (two 32-bit words) to two float pairs.
+__device__ __forceinline__ void unpack4(uint2 u, float2& a, float2& b) {
+  a = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+  b = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
-// Sum v[0..3] over the 16 lanes of a half-warp; on return lane m holds the
-// full sum of slot (m >> 2).
-__device__ __forceinline__ float transpose_reduce4(const float (&v)[4], int m) {
-  const bool u3 = m & 8, u2 = m & 4;
-  float a[2];
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
+// Sum the V values of every lane over the 16 lanes of a half-warp.  On
+// return lane m holds kOut = max(1, V / 16) full sums v[0..kOut), which are
+// the original indices (m / kDup) * kOut + k, kDup = max(1, 16 / V).
+template <int V>
+__device__ __forceinline__ void transpose_reduce(float (&v)[V], int m) {
+  int n = V;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = u3 ? v[i] : v[i + 2];
-    const float keep = u3 ? v[i + 2] : v[i];
-    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  for (int b = 3; b >= 0; --b) {
+    const int sh = 1 << b;
+    if (n > 1) {
+      const bool up = (m >> b) & 1;
+      const int hf = n / 2;
+#pragma unroll
+      for (int k = 0; k < V / 2; ++k) {
+        if (k < hf) {
+          const float send = up ? v[k] : v[k + hf];
+          const float keep = up ? v[k + hf] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
+        }
+      }
+      n = hf;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], sh);
+    }
   }
-  const float send = u2 ? a[0] : a[1];
-  const float keep = u2 ? a[1] : a[0];
-  float c = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  c += __shfl_xor_sync(0xffffffffu, c, 2);
-  c += __shfl_xor_sync(0xffffffffu, c, 1);
-  return c;
 }
 
 template <int GQ>
 __global__ void __launch_bounds__(256, 1)
 decode_partial_kernel(DecodeKParams p) {
+  constexpr int kV = GQ * kSlots;                 // scores per half-warp per step
+  constexpr int kOut = kV >= 16 ? kV / 16 : 1;    // sums held per lane after the reduction
+  constexpr int kDup = kV >= 16 ? 1 : 16 / kV;    // lanes holding the same sum
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* s_qa = reinterpret_cast<float*>(smem_raw);              // [Hq][128], pre-scaled
   float* s_qr = s_qa + p.Hq * kD;                                // [Hq][128]
   float2* s_offs = reinterpret_cast<float2*>(s_qr + p.Hq * kD);  // [65][64]: R_{-n}
-  float2* s_cs = s_offs + (kBlockKeys + 1) * 64;                 // [64][64]: this block
-  float2* s_base = s_cs + kBlockKeys * 64;                       // [64]
-  float2* s_pow = s_base + 64;                                   // [7][64]: R_{-2^b}
-  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_pow + 7 * 64);  // [warps][stages]
+  float* s_c = reinterpret_cast<float*>(s_offs + (kBlockKeys + 1) * 64);  // [64][64] cos
+  float* s_s = s_c + kBlockKeys * 64;                                     // [64][64] sin
+  float2* s_base = reinterpret_cast<float2*>(s_s + kBlockKeys * 64);      // [64]
+  float2* s_pow = s_base + 64;                                            // [7][64]: R_{-2^b}
+  float* s_x = reinterpret_cast<float*>(s_pow + 7 * 64);  // per warp: z[GQ][8], p[8][GQ], alpha[GQ]
+  unsigned char* s_ring =
+      reinterpret_cast<unsigned char*>(s_x + (blockDim.x / 32) * exchange_floats(GQ));
   __shared__ float2 s_qcs[2][64];
+
+  // Let the merge kernel (a programmatic dependent) launch early; it waits
+  // for this grid's completion before reading the partials.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -126,6 +155,9 @@ decode_partial_kernel(DecodeKParams p) {
   const __nv_bfloat16* vbase = p.vc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(s_ring)) +
                         static_cast<uint32_t>(warp * kStages * kStageBytes);
+  float* xz = s_x + warp * exchange_floats(GQ);  // z[GQ][8]
+  float* xp = xz + 8 * GQ;             // p[8][GQ]
+  float* xa = xp + 8 * GQ;             // alpha[GQ]
   const int nsteps = (je - js + kStep - 1) / kStep;
 
   // Stage layout: K rows of the step's 8 keys (256 B each), then V rows.
@@ -199,14 +231,20 @@ decode_partial_kernel(DecodeKParams p) {
   }
   __syncthreads();
 
-  float o[GQ][8];
-  float m_run[GQ], l_part[GQ];
+  // Accumulators: o[h][0..3] = elements (4m, 4m+1), (4m+2, 4m+3),
+  // (64+4m, 64+4m+1), (64+4m+2, 64+4m+3) of head h, keys of parity `half`.
+  float2 o[GQ][4];
 #pragma unroll
-  for (int h = 0; h < GQ; ++h) {
-    m_run[h] = -INFINITY;
-    l_part[h] = 0.f;
+  for (int h = 0; h < GQ; ++h)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+    for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
+  // Softmax state of the (head, key) pairs this lane owns in the exchange.
+  constexpr int kOwn = (GQ * 8 + 31) / 32;
+  float m_run[kOwn], l_run[kOwn];
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) {
+    m_run[k] = -INFINITY;
+    l_run[k] = 0.f;
   }
 
   for (int it = 0; it < nsteps; ++it) {
@@ -225,7 +263,9 @@ decode_partial_kernel(DecodeKParams p) {
       for (int idx = tid; idx < kBlockKeys * 64; idx += nthr) {
         const int t = idx / 64, i = idx % 64;
         const int n = t - (alias(j0 + t, p.G) - fj0);
-        s_cs[idx] = compose(s_base[i], s_offs[n * 64 + i]);
+        const float2 cs = compose(s_base[i], s_offs[n * 64 + i]);
+        s_c[idx] = cs.x;
+        s_s[idx] = cs.y;
       }
       __syncthreads();
     }
@@ -237,147 +277,245 @@ decode_partial_kernel(DecodeKParams p) {
     const unsigned char* st = s_ring + (warp * kStages + it % kStages) * kStageBytes;
     const bool all_local = !bifocal || jstep >= first_local;
     const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
-    float z[GQ];
-    auto scores = [&](const float* qs, bool rot, float (&out)[GQ]) {
-      float sc[GQ][kSlots];
-      float qlo[GQ][4], qhi[GQ][4];
+
+    // Partial scores sc[h * 4 + s] for key 2s + half of this step.
+    auto scores = [&](const float* qs, bool rot, float (&sc)[kV]) {
+      float2 qa[GQ][4];
 #pragma unroll
       for (int h = 0; h < GQ; ++h) {
         const float4 a = *reinterpret_cast<const float4*>(qs + (hk * GQ + h) * kD + 4 * m);
         const float4 c = *reinterpret_cast<const float4*>(qs + (hk * GQ + h) * kD + 64 + 4 * m);
-        qlo[h][0] = a.x; qlo[h][1] = a.y; qlo[h][2] = a.z; qlo[h][3] = a.w;
-        qhi[h][0] = c.x; qhi[h][1] = c.y; qhi[h][2] = c.z; qhi[h][3] = c.w;
+        qa[h][0] = make_float2(a.x, a.y);
+        qa[h][1] = make_float2(a.z, a.w);
+        qa[h][2] = make_float2(c.x, c.y);
+        qa[h][3] = make_float2(c.z, c.w);
       }
 #pragma unroll
       for (int s = 0; s < kSlots; ++s) {
         const int key = 2 * s + half;
-        const uint2 klo = *reinterpret_cast<const uint2*>(st + key * 256 + 8 * m);
-        const uint2 khi = *reinterpret_cast<const uint2*>(st + key * 256 + 128 + 8 * m);
-        float x[4], y[4];
-        unpack4(klo, x);
-        unpack4(khi, y);
+        float2 x01, x23, y01, y23;
+        unpack4(*reinterpret_cast<const uint2*>(st + key * 256 + 8 * m), x01, x23);
+        unpack4(*reinterpret_cast<const uint2*>(st + key * 256 + 128 + 8 * m), y01, y23);
         if (rot) {
           const int t = (jstep - j0) + key;
-          const float4 c01 = *reinterpret_cast<const float4*>(s_cs + t * 64 + 4 * m);
-          const float4 c23 = *reinterpret_cast<const float4*>(s_cs + t * 64 + 4 * m + 2);
-          const float2 cs[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
-                                make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const float2 r = rotate_pair(x[f], y[f], cs[f]);
-            x[f] = r.x;
-            y[f] = r.y;
-          }
+          const float4 c = *reinterpret_cast<const float4*>(s_c + t * 64 + 4 * m);
+          const float4 sn = *reinterpret_cast<const float4*>(s_s + t * 64 + 4 * m);
+          const float2 c01 = make_float2(c.x, c.y), c23 = make_float2(c.z, c.w);
+          const float2 s01 = make_float2(sn.x, sn.y), s23 = make_float2(sn.z, sn.w);
+          // (x, y) -> (x c - y s, y c + x s)
+          const float2 nx01 = __ffma2_rn(y01, neg2(s01), __fmul2_rn(x01, c01));
+          const float2 nx23 = __ffma2_rn(y23, neg2(s23), __fmul2_rn(x23, c23));
+          y01 = __ffma2_rn(x01, s01, __fmul2_rn(y01, c01));
+          y23 = __ffma2_rn(x23, s23, __fmul2_rn(y23, c23));
+          x01 = nx01;
+          x23 = nx23;
         }
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-          float acc = 0.f;
-#pragma unroll
-          for (int f = 0; f < 4; ++f) acc = fmaf(qlo[h][f], x[f], fmaf(qhi[h][f], y[f], acc));
-          sc[h][s] = acc;
+          float2 acc = __fmul2_rn(qa[h][0], x01);
+          acc = __ffma2_rn(qa[h][1], x23, acc);
+          acc = __ffma2_rn(qa[h][2], y01, acc);
+          acc = __ffma2_rn(qa[h][3], y23, acc);
+          sc[h * kSlots + s] = acc.x + acc.y;
         }
       }
-#pragma unroll
-      for (int h = 0; h < GQ; ++h) out[h] = transpose_reduce4(sc[h], m);
+      transpose_reduce<kV>(sc, m);
     };
+
+    float z[kV];
     if (all_local) {
       scores(s_qa, false, z);
     } else if (all_remote) {
       scores(s_qr, true, z);
     } else {
-      float zr[GQ];
+      float zr[kV];
       scores(s_qa, false, z);
       scores(s_qr, true, zr);
-      const int j = jstep + 2 * (m >> 2) + half;
 #pragma unroll
-      for (int h = 0; h < GQ; ++h)
-        if (j < first_local) z[h] = zr[h];
-    }
-    const int jmine = jstep + 2 * (m >> 2) + half;
-    const bool valid = jmine < je;
-    float pr[GQ];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-      const float zz = valid ? z[h] : -INFINITY;
-      float bm = zz;
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-      const float m_new = fmaxf(m_run[h], bm);
-      const float alpha = exp2f(m_run[h] - m_new);
-      m_run[h] = m_new;
-      pr[h] = exp2f(zz - m_new);
-      l_part[h] = l_part[h] * alpha + ((m & 3) ? 0.f : pr[h]);
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+      for (int k = 0; k < kOut; ++k) {
+        const int i = (m / kDup) * kOut + k;  // = h * 4 + s
+        const int j = jstep + 2 * (i % kSlots) + half;
+        if (j < first_local) z[k] = zr[k];
       }
     }
+    // Publish the step's scores: xz[h][key].
+#pragma unroll
+    for (int k = 0; k < kOut; ++k) {
+      const int i = (m / kDup) * kOut + k;
+      xz[(i / kSlots) * 8 + 2 * (i % kSlots) + half] = z[k];
+    }
+    __syncwarp();
+    // Online softmax, one lane per (head, key); the 8 keys of a head are 8
+    // consecutive lanes.
+    bool any_rescale = false;
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+      const int idx = k * 32 + lane;
+      const bool own = idx < GQ * 8;
+      const int h = idx >> 3, key = idx & 7;
+      const bool valid = own && (jstep + key < je);
+      const float zz = valid ? xz[idx] : -INFINITY;
+      float bm = zz;
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      float alpha = 1.f;
+      if (bm > m_run[k] + kRescaleThreshold) {  // raise the max lazily
+        alpha = exp2f(m_run[k] - bm);
+        m_run[k] = bm;
+      }
+      const float mexp = m_run[k] == -INFINITY ? 0.f : m_run[k];
+      const float pr = exp2f(zz - mexp);
+      l_run[k] = l_run[k] * alpha + pr;
+      if (own) {
+        xp[key * GQ + h] = pr;
+        if (key == 0) xa[h] = alpha;
+      }
+      any_rescale |= alpha != 1.f;
+    }
+    any_rescale = __any_sync(0xffffffffu, any_rescale);
+    __syncwarp();
+    if (any_rescale) {
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        const float a = xa[h];
+        const float2 a2 = make_float2(a, a);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
+      }
+    }
+    // O += P V
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
       const int key = 2 * s + half;
-      const uint2 vlo = *reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 8 * m);
-      const uint2 vhi = *reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 128 + 8 * m);
-      float x[4], y[4];
-      unpack4(vlo, x);
-      unpack4(vhi, y);
+      float2 v01, v23, w01, w23;
+      unpack4(*reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 8 * m), v01, v23);
+      unpack4(*reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 128 + 8 * m), w01, w23);
+      float pk[GQ];
+      if constexpr (GQ % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < GQ; h += 4) {
+          const float4 q4 = *reinterpret_cast<const float4*>(xp + key * GQ + h);
+          pk[h] = q4.x;
+          pk[h + 1] = q4.y;
+          pk[h + 2] = q4.z;
+          pk[h + 3] = q4.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) pk[h] = xp[key * GQ + h];
+      }
 #pragma unroll
       for (int h = 0; h < GQ; ++h) {
-        const float ps = __shfl_sync(0xffffffffu, pr[h], half * 16 + 4 * s);
-#pragma unroll
-        for (int f = 0; f < 4; ++f) {
-          o[h][f] = fmaf(ps, x[f], o[h][f]);
-          o[h][4 + f] = fmaf(ps, y[f], o[h][4 + f]);
-        }
+        const float2 p2 = make_float2(pk[h], pk[h]);
+        o[h][0] = __ffma2_rn(p2, v01, o[h][0]);
+        o[h][1] = __ffma2_rn(p2, v23, o[h][1]);
+        o[h][2] = __ffma2_rn(p2, w01, o[h][2]);
+        o[h][3] = __ffma2_rn(p2, w23, o[h][3]);
       }
     }
-    __syncwarp();  // the stage is refilled by the next issue_step
+    __syncwarp();  // the stage and the exchange buffer are rewritten next step
   }
   cp_async_wait<0>();
 
   if (!active) return;
-  // Combine the two key parities and the 16-lane partial sums.
+  // Per-head statistics: the owner lanes of a head share m; l sums over keys.
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) {
+    float l = l_run[k];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    const int idx = k * 32 + lane;
+    if (idx < GQ * 8 && (idx & 7) == 0) {
+      const int hq = hk * GQ + (idx >> 3);
+      const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
+      p.part_ml[slot * 2] = m_run[k];
+      p.part_ml[slot * 2 + 1] = l;
+    }
+  }
+  // Combine the two key parities.
 #pragma unroll
   for (int h = 0; h < GQ; ++h) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 16);
-    float l = l_part[h];
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    const int hq = hk * GQ + h;
-    const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
-    if (half == 0) {
-      float* dst = p.part_o + slot * kD;
-      *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-      *reinterpret_cast<float4*>(dst + 64 + 4 * m) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+    for (int e = 0; e < 4; ++e) {
+      o[h][e].x += __shfl_xor_sync(0xffffffffu, o[h][e].x, 16);
+      o[h][e].y += __shfl_xor_sync(0xffffffffu, o[h][e].y, 16);
     }
-    if (lane == 0) {
-      p.part_ml[slot * 2] = m_run[h];
-      p.part_ml[slot * 2 + 1] = l;
+    if (half == 0) {
+      const int hq = hk * GQ + h;
+      const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
+      float* dst = p.part_o + slot * kD;
+      *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+      *reinterpret_cast<float4*>(dst + 64 + 4 * m) =
+          make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
     }
   }
 }
 
-// Merge the per-slice partials of one (batch, query head): log-sum-exp
-// weights exp2(m_s - M), output sum_s w_s o_s / sum_s w_s l_s.
-__global__ void __launch_bounds__(128)
+// Merge the per-slice partials of one (batch, query head) with log-sum-exp
+// weights w_s = exp2(m_s - M): out = sum_s w_s o_s / sum_s w_s l_s.  Eight
+// warps split the slices; a lane owns four output elements.
+__global__ void __launch_bounds__(256)
 decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                     int nsplit, int BH, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  const int bh = blockIdx.x, e = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[(static_cast<long long>(s) * BH + bh) * 2]);
-  float num = 0.f, den = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[8];
+  __shared__ float4 s_acc[8][32];
+  // The partials are written by the preceding grid.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float mx = -INFINITY;
+  for (int s = tid; s < nsplit; s += 256) mx = fmaxf(mx, part_ml[(static_cast<long long>(s) * BH + bh) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  float M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
+  __syncthreads();
+  float den = 0.f;
+  for (int s = tid; s < nsplit; s += 256) {
     const long long slot = static_cast<long long>(s) * BH + bh;
     const float w = exp2f(part_ml[slot * 2] - M);
+    s_w[s] = w;
     den = fmaf(w, part_ml[slot * 2 + 1], den);
-    num = fmaf(w, part_o[slot * kD + e], num);
   }
-  out[static_cast<long long>(bh) * kD + e] = __float2bfloat16_rn(num / den);
-  if (lse != nullptr && e == 0) lse[bh] = (M + log2f(den)) * 0.69314718055994531f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) s_red[warp] = den;
+  __syncthreads();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = warp; s < nsplit; s += 8) {
+    const float w = s_w[s];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + (static_cast<long long>(s) * BH + bh) * kD + 4 * lane);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  s_acc[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float D = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) D += s_red[w];
+    float4 t = s_acc[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      t.x += s_acc[w][lane].x;
+      t.y += s_acc[w][lane].y;
+      t.z += s_acc[w][lane].z;
+      t.w += s_acc[w][lane].w;
+    }
+    const float inv = 1.f / D;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + static_cast<long long>(bh) * kD + 4 * lane);
+    dst[0] = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+    dst[1] = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+    if (lse != nullptr && lane == 0) lse[bh] = (M + log2f(D)) * 0.69314718055994531f;
+  }
 }
 
 int num_sms() {
@@ -420,8 +558,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
   const int warps = std::max(a.Hkv, 1);
   const size_t smem = static_cast<size_t>(2) * a.Hq * kD * sizeof(float) +
-                      static_cast<size_t>((kBlockKeys + 1) * 64 + kBlockKeys * 64 + 64 + 7 * 64) *
-                          sizeof(float2) +
+                      static_cast<size_t>((kBlockKeys + 1) * 64 + 64 + 7 * 64) * sizeof(float2) +
+                      static_cast<size_t>(2) * kBlockKeys * 64 * sizeof(float) +
+                      static_cast<size_t>(warps) * exchange_floats(GQ) * sizeof(float) +
                       static_cast<size_t>(warps) * kStages * kStageBytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   const dim3 grid(nsplit, a.B);
@@ -444,9 +583,22 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 #undef JL_DECODE_CASE
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  decode_merge_kernel<<<a.B * a.Hq, kD, 0, stream>>>(p.part_o, p.part_ml, nsplit, a.B * a.Hq,
-                                                     static_cast<__nv_bfloat16*>(a.o), a.lse);
-  return cudaGetLastError();
+
+  // The merge waits on the partial kernel through griddepcontrol.wait, so it
+  // may be launched before that kernel finishes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hq);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, static_cast<const float*>(p.part_o),
+                            static_cast<const float*>(p.part_ml), nsplit, a.B * a.Hq,
+                            static_cast<__nv_bfloat16*>(a.o), a.lse);
 }
 
 }  // namespace jl

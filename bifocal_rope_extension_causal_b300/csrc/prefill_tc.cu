@@ -313,9 +313,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
           if (!keep) s[c] = -INFINITY;
         }
       }
-      float mx = s[0];
+      // Row max and row sum as 8-way trees (independent chains).
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[c + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_used, mx * sc);
       float factor = 1.f;
       if (m_new > m_used + kRescaleThreshold) {
@@ -323,24 +330,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
         m_used = m_new;
       }
       const float m_exp = (m_used == -INFINITY) ? 0.f : m_used;
-      float rowsum = 0.f;
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_exp, -m_exp);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
       uint32_t pk0[32], pk1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2_approx(fmaf(s[2 * i], sc, -m_exp));
-        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, -m_exp));
-        rowsum += p0 + p1;
-        pk0[i] = pack_bf16x2(p0, p1);
+        const float2 a = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
+        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+        pk0[i] = pack_bf16x2(e.x, e.y);
       }
+      tmem_st32(tS + 0, pk0);  // P columns 0..31 over S columns already read
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2_approx(fmaf(s[64 + 2 * i], sc, -m_exp));
-        const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], sc, -m_exp));
-        rowsum += p0 + p1;
-        pk1[i] = pack_bf16x2(p0, p1);
+        const float2 a = __ffma2_rn(make_float2(s[64 + 2 * i], s[64 + 2 * i + 1]), sc2, nm2);
+        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+        pk1[i] = pack_bf16x2(e.x, e.y);
       }
+      const float2 t2 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+      const float rowsum = t2.x + t2.y;
       l_run = l_run * factor + rowsum;
-      tmem_st32(tS + 0, pk0);
       tmem_st32(tS + 32, pk1);
       // Rescale O_t in tensor memory when any row of this warp raised its max.
       if (v > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
