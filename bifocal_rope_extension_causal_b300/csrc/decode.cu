@@ -14,10 +14,10 @@
 // launched as a programmatic dependent of the first, merges the slices with
 // log-sum-exp weights.
 //
-// Memory path.  Each warp streams its head's K and V rows (256 B each per
-// key) through its own 3-stage shared-memory ring with 16-byte cp.async
-// copies (16 lanes per row: fully coalesced), so the bytes in flight do not
-// depend on registers; keys past the slice end are zero-filled.
+// Memory path.  kWarpsPerHead warps per KV head take alternate 8-key steps;
+// each streams its head's K and V rows (256 B each per key) through its own
+// kStages-deep shared-memory ring with 16-byte cp.async copies (16 lanes per
+// row: fully coalesced; keys past the slice end are zero-filled).
 //
 // Rotation accuracy.  Delta(j) reaches ~1e5, so its angle is reduced in
 // double precision once per CTA (first block); later blocks step the base
@@ -50,7 +50,8 @@ constexpr int kD = 128;
 constexpr int kBlockKeys = 64;  // keys per rotation-table block
 constexpr int kStep = 8;        // keys per warp step
 constexpr int kSlots = kStep / 2;
-constexpr int kStages = 3;      // per-warp ring depth
+constexpr int kStages = 2;      // per-warp ring depth
+constexpr int kWarpsPerHead = 2;  // warps sharing a KV head (alternate steps)
 constexpr int kMaxSplits = 512;
 constexpr int kStageBytes = kStep * 2 * kD * 2;  // K and V rows of one step
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
@@ -116,22 +117,24 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[V], int m) {
 }
 
 template <int GQ>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
 decode_partial_kernel(DecodeKParams p) {
   constexpr int kV = GQ * kSlots;                 // scores per half-warp per step
   constexpr int kOut = kV >= 16 ? kV / 16 : 1;    // sums held per lane after the reduction
   constexpr int kDup = kV >= 16 ? 1 : 16 / kV;    // lanes holding the same sum
+  constexpr int kOwn = (GQ * 8 + 31) / 32;        // (head, key) pairs per lane in the softmax
+  constexpr int kBlockSteps = kBlockKeys / kStep;  // global steps per table block (8)
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* s_qa = reinterpret_cast<float*>(smem_raw);              // [Hq][128], pre-scaled
-  float* s_qr = s_qa + p.Hq * kD;                                // [Hq][128]
-  float2* s_offs = reinterpret_cast<float2*>(s_qr + p.Hq * kD);  // [65][64]: R_{-n}
-  float* s_c = reinterpret_cast<float*>(s_offs + (kBlockKeys + 1) * 64);  // [64][64] cos
-  float* s_s = s_c + kBlockKeys * 64;                                     // [64][64] sin
-  float2* s_base = reinterpret_cast<float2*>(s_s + kBlockKeys * 64);      // [64]
-  float2* s_pow = s_base + 64;                                            // [7][64]: R_{-2^b}
-  float* s_x = reinterpret_cast<float*>(s_pow + 7 * 64);  // per warp: z[GQ][8], p[8][GQ], alpha[GQ]
-  unsigned char* s_ring =
-      reinterpret_cast<unsigned char*>(s_x + (blockDim.x / 32) * exchange_floats(GQ));
+  const int nwarps = blockDim.x >> 5;
+  float* s_qa = reinterpret_cast<float*>(smem_raw);                 // [Hq][128], pre-scaled
+  float* s_qr = s_qa + p.Hq * kD;                                   // [Hq][128]
+  float* s_c = s_qr + p.Hq * kD;                                    // [64 keys][64] cos
+  float* s_s = s_c + kBlockKeys * 64;                               // [64 keys][64] sin
+  float2* s_lo = reinterpret_cast<float2*>(s_s + kBlockKeys * 64);  // [8][64]: R_{-b}
+  float2* s_hi = s_lo + 8 * 64;                                     // [9][64]: R_{-8a}
+  float2* s_base = s_hi + 9 * 64;                                   // [64]
+  float* s_x = reinterpret_cast<float*>(s_base + 64);               // per-warp exchange buffers
+  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_x + nwarps * exchange_floats(GQ));
   __shared__ float2 s_qcs[2][64];
 
   // Let the merge kernel (a programmatic dependent) launch early; it waits
@@ -148,23 +151,26 @@ decode_partial_kernel(DecodeKParams p) {
   const bool bifocal = p.G > 1;
   const int first_local = qpos - p.w0;  // keys j >= first_local are local
 
-  const int hk = warp;
-  const bool active = hk < p.Hkv;
+  // kWarpsPerHead warps per KV head: warp `par` of a head takes the global
+  // steps it = kWarpsPerHead * u + par.
+  const int hk = warp % p.Hkv, par = warp / p.Hkv;
   const long long row_stride = static_cast<long long>(p.Hkv) * kD;
   const __nv_bfloat16* kbase = p.kc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
   const __nv_bfloat16* vbase = p.vc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
-  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(s_ring)) +
-                        static_cast<uint32_t>(warp * kStages * kStageBytes);
+  unsigned char* my_ring = s_ring + warp * kStages * kStageBytes;
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(my_ring));
   float* xz = s_x + warp * exchange_floats(GQ);  // z[GQ][8]
-  float* xp = xz + 8 * GQ;             // p[8][GQ]
-  float* xa = xp + 8 * GQ;             // alpha[GQ]
+  float* xp = xz + 8 * GQ;                       // p[8][GQ]
+  float* xa = xp + 8 * GQ;                       // alpha[GQ]
   const int nsteps = (je - js + kStep - 1) / kStep;
+  const int nlocal = (nsteps + kWarpsPerHead - 1) / kWarpsPerHead;  // local steps (warp 0 of a head)
 
   // Stage layout: K rows of the step's 8 keys (256 B each), then V rows.
-  auto issue_step = [&](int it) {
-    if (active && it < nsteps) {
+  auto issue_step = [&](int u) {
+    const int it = kWarpsPerHead * u + par;
+    if (it < nsteps) {
       const int jstep = js + it * kStep;
-      const uint32_t st = ring + static_cast<uint32_t>((it % kStages) * kStageBytes);
+      const uint32_t st = ring + static_cast<uint32_t>((u % kStages) * kStageBytes);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int idx = i * 32 + lane;  // 256 chunks of 16 B
@@ -178,41 +184,29 @@ decode_partial_kernel(DecodeKParams p) {
     }
     cp_async_commit();
   };
-  // Start the stream before the set-up work below.
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) issue_step(s);
 
-  // Query rotations: R_{L-1} x_q and R_{f(L-1)} x_q, times scale * log2(e).
+  // Query rotations R_{L-1} and R_{f(L-1)}, and the small rotation tables.
   for (int i = tid; i < 64; i += nthr) {
     s_qcs[0][i] = rope_cos_sin(qpos, p.freqs.w[i]);
     s_qcs[1][i] = rope_cos_sin(alias(qpos, p.G), p.freqs.w[i]);
   }
   const bool any_remote = bifocal && js < first_local;
   if (any_remote) {
-    // R_{-2^b}, b = 0..6, from the frequency split omega = hi + lo with hi
-    // holding 17 significant bits (so 2^b * hi is exact in float).
-    for (int idx = tid; idx < 7 * 64; idx += nthr) {
-      const int bb = idx / 64, i = idx % 64;
+    // R_{-b} (b < 8) and R_{-8a} (a <= 8) with omega = hi + lo, hi holding
+    // 17 significant bits so that n * hi is exact in float for n <= 64.
+    for (int idx = tid; idx < 17 * 64; idx += nthr) {
+      const int r = idx / 64, i = idx % 64;
+      const int n = r < 8 ? r : 8 * (r - 8);
       const double w = p.freqs.w[i];
       const float whi = __uint_as_float(__float_as_uint(static_cast<float>(w)) & 0xffffff80u);
       const float wlo = static_cast<float>(w - static_cast<double>(whi));
-      const float n = static_cast<float>(1 << bb);
       float sn, cn;
-      sincosf(n * whi, &sn, &cn);
-      const float e = n * wlo;  // |e| < 1e-3: second-order small-angle rotation
-      const float2 r = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
-      s_pow[idx] = make_float2(r.x, -r.y);  // R_{-2^b}
-    }
-    for (int i = tid; i < 64; i += nthr) s_offs[i] = make_float2(1.f, 0.f);
-    __syncthreads();
-    // R_{-n} = R_{-(n - 2^b)} R_{-2^b}, b = top bit of n, built layer by layer.
-    for (int bb = 0; bb < 7; ++bb) {
-      const int lo = 1 << bb, cnt = min(lo, kBlockKeys + 1 - lo);
-      for (int idx = tid; idx < cnt * 64; idx += nthr) {
-        const int n = lo + idx / 64, i = idx % 64;
-        s_offs[n * 64 + i] = compose(s_offs[(n - lo) * 64 + i], s_pow[bb * 64 + i]);
-      }
-      __syncthreads();
+      sincosf(static_cast<float>(n) * whi, &sn, &cn);
+      const float e = static_cast<float>(n) * wlo;  // |e| < 1e-3
+      const float2 rr = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
+      (r < 8 ? s_lo : s_hi)[(r < 8 ? r : r - 8) * 64 + i] = make_float2(rr.x, -rr.y);  // R_{-n}
     }
     for (int i = tid; i < 64; i += nthr) s_base[i] = rope_cos_sin(alias_offset(js, p.G), p.freqs.w[i]);
   }
@@ -229,17 +223,13 @@ decode_partial_kernel(DecodeKParams p) {
     s_qr[h * kD + i] = rr.x * p.scale_log2;
     s_qr[h * kD + 64 + i] = rr.y * p.scale_log2;
   }
-  __syncthreads();
+  // (The first table build below starts with a barrier.)
 
-  // Accumulators: o[h][0..3] = elements (4m, 4m+1), (4m+2, 4m+3),
-  // (64+4m, 64+4m+1), (64+4m+2, 64+4m+3) of head h, keys of parity `half`.
   float2 o[GQ][4];
 #pragma unroll
   for (int h = 0; h < GQ; ++h)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
-  // Softmax state of the (head, key) pairs this lane owns in the exchange.
-  constexpr int kOwn = (GQ * 8 + 31) / 32;
   float m_run[kOwn], l_run[kOwn];
 #pragma unroll
   for (int k = 0; k < kOwn; ++k) {
@@ -247,49 +237,45 @@ decode_partial_kernel(DecodeKParams p) {
     l_run[k] = 0.f;
   }
 
-  for (int it = 0; it < nsteps; ++it) {
-    const int jstep = js + it * kStep;
-    const int j0 = js + (it / (kBlockKeys / kStep)) * kBlockKeys;  // block base
-    if ((it % (kBlockKeys / kStep)) == 0 && bifocal && j0 < first_local) {
-      // Rotation table of this 64-key block: cs[t] = base(j0) R_{-n(t)}.
-      __syncthreads();
-      if (j0 != js) {
-        const int jp = j0 - kBlockKeys;  // advance the base from the previous block
-        const int n = alias_offset(jp, p.G) - alias_offset(j0, p.G);
-        for (int i = tid; i < 64; i += nthr) s_base[i] = compose(s_base[i], s_offs[n * 64 + i]);
-      }
-      __syncthreads();
-      const int fj0 = alias(j0, p.G);
-      for (int idx = tid; idx < kBlockKeys * 64; idx += nthr) {
-        const int t = idx / 64, i = idx % 64;
-        const int n = t - (alias(j0 + t, p.G) - fj0);
-        const float2 cs = compose(s_base[i], s_offs[n * 64 + i]);
-        s_c[idx] = cs.x;
-        s_s[idx] = cs.y;
+  constexpr int kBlockLocal = kBlockSteps / kWarpsPerHead;  // local steps per table block
+  for (int u = 0; u < nlocal; ++u) {
+    const int it = kWarpsPerHead * u + par;
+    const int blk = u / kBlockLocal;
+    const int j0 = js + blk * kBlockKeys;  // table block base
+    if ((u % kBlockLocal) == 0) {
+      __syncthreads();  // previous table no longer read; q (first pass) written
+      if (bifocal && j0 < first_local) {
+        if (blk > 0) {
+          const int n = alias_offset(j0 - kBlockKeys, p.G) - alias_offset(j0, p.G);  // 0..64
+          for (int i = tid; i < 64; i += nthr)
+            s_base[i] = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
+          __syncthreads();
+        }
+        const int fj0 = alias(j0, p.G);
+        for (int idx = tid; idx < kBlockKeys * 64; idx += nthr) {
+          const int t = idx / 64, i = idx % 64;
+          const int n = t - (alias(j0 + t, p.G) - fj0);  // 0..63
+          const float2 cs = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
+          s_c[idx] = cs.x;
+          s_s[idx] = cs.y;
+        }
       }
       __syncthreads();
     }
-    issue_step(it + kStages - 1);
+    issue_step(u + kStages - 1);
     cp_async_wait<kStages - 1>();
     __syncwarp();
-    if (!active) continue;
+    if (it >= nsteps) continue;
 
-    const unsigned char* st = s_ring + (warp * kStages + it % kStages) * kStageBytes;
+    const int jstep = js + it * kStep;
+    const unsigned char* st = my_ring + (u % kStages) * kStageBytes;
     const bool all_local = !bifocal || jstep >= first_local;
     const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
 
-    // Partial scores sc[h * 4 + s] for key 2s + half of this step.
-    auto scores = [&](const float* qs, bool rot, float (&sc)[kV]) {
-      float2 qa[GQ][4];
-#pragma unroll
-      for (int h = 0; h < GQ; ++h) {
-        const float4 a = *reinterpret_cast<const float4*>(qs + (hk * GQ + h) * kD + 4 * m);
-        const float4 c = *reinterpret_cast<const float4*>(qs + (hk * GQ + h) * kD + 64 + 4 * m);
-        qa[h][0] = make_float2(a.x, a.y);
-        qa[h][1] = make_float2(a.z, a.w);
-        qa[h][2] = make_float2(c.x, c.y);
-        qa[h][3] = make_float2(c.z, c.w);
-      }
+    // Full scores of this step's keys; lane m ends with sums (m/kDup)*kOut+k
+    // of the index h * 4 + s (key 2s + half).
+    auto scores = [&](const float* qs, bool rot, float (&zout)[kOut]) {
+      float sc[kV];
 #pragma unroll
       for (int s = 0; s < kSlots; ++s) {
         const int key = 2 * s + half;
@@ -312,30 +298,34 @@ decode_partial_kernel(DecodeKParams p) {
         }
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-          float2 acc = __fmul2_rn(qa[h][0], x01);
-          acc = __ffma2_rn(qa[h][1], x23, acc);
-          acc = __ffma2_rn(qa[h][2], y01, acc);
-          acc = __ffma2_rn(qa[h][3], y23, acc);
+          const float* qh = qs + (hk * GQ + h) * kD;
+          const float4 a = *reinterpret_cast<const float4*>(qh + 4 * m);
+          const float4 c = *reinterpret_cast<const float4*>(qh + 64 + 4 * m);
+          float2 acc = __fmul2_rn(make_float2(a.x, a.y), x01);
+          acc = __ffma2_rn(make_float2(a.z, a.w), x23, acc);
+          acc = __ffma2_rn(make_float2(c.x, c.y), y01, acc);
+          acc = __ffma2_rn(make_float2(c.z, c.w), y23, acc);
           sc[h * kSlots + s] = acc.x + acc.y;
         }
       }
       transpose_reduce<kV>(sc, m);
+#pragma unroll
+      for (int k = 0; k < kOut; ++k) zout[k] = sc[k];
     };
 
-    float z[kV];
+    float z[kOut];
     if (all_local) {
       scores(s_qa, false, z);
     } else if (all_remote) {
       scores(s_qr, true, z);
     } else {
-      float zr[kV];
+      float zr[kOut];
       scores(s_qa, false, z);
       scores(s_qr, true, zr);
 #pragma unroll
       for (int k = 0; k < kOut; ++k) {
         const int i = (m / kDup) * kOut + k;  // = h * 4 + s
-        const int j = jstep + 2 * (i % kSlots) + half;
-        if (j < first_local) z[k] = zr[k];
+        if (jstep + 2 * (i % kSlots) + half < first_local) z[k] = zr[k];
       }
     }
     // Publish the step's scores: xz[h][key].
@@ -345,8 +335,9 @@ decode_partial_kernel(DecodeKParams p) {
       xz[(i / kSlots) * 8 + 2 * (i % kSlots) + half] = z[k];
     }
     __syncwarp();
-    // Online softmax, one lane per (head, key); the 8 keys of a head are 8
-    // consecutive lanes.
+    // Online softmax, one lane per (head, key); a head's 8 keys are 8
+    // consecutive lanes.  The max used for the exponentials is raised only
+    // when it grows by more than kRescaleThreshold.
     bool any_rescale = false;
 #pragma unroll
     for (int k = 0; k < kOwn; ++k) {
@@ -360,7 +351,7 @@ decode_partial_kernel(DecodeKParams p) {
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
       float alpha = 1.f;
-      if (bm > m_run[k] + kRescaleThreshold) {  // raise the max lazily
+      if (bm > m_run[k] + kRescaleThreshold) {
         alpha = exp2f(m_run[k] - bm);
         m_run[k] = bm;
       }
@@ -384,7 +375,7 @@ decode_partial_kernel(DecodeKParams p) {
         for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
       }
     }
-    // O += P V
+    // O += P V (keys past the slice end have p = 0 and zero-filled rows).
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
       const int key = 2 * s + half;
@@ -418,103 +409,163 @@ decode_partial_kernel(DecodeKParams p) {
   }
   cp_async_wait<0>();
 
-  if (!active) return;
-  // Per-head statistics: the owner lanes of a head share m; l sums over keys.
+  // Per-head statistics of this warp: m (shared by the head's 8 lanes) and
+  // l summed over them; combine the two key parities of o within the warp.
+  float mh[kOwn], lh[kOwn];
 #pragma unroll
   for (int k = 0; k < kOwn; ++k) {
     float l = l_run[k];
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     l += __shfl_xor_sync(0xffffffffu, l, 4);
-    const int idx = k * 32 + lane;
-    if (idx < GQ * 8 && (idx & 7) == 0) {
-      const int hq = hk * GQ + (idx >> 3);
-      const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
-      p.part_ml[slot * 2] = m_run[k];
-      p.part_ml[slot * 2 + 1] = l;
-    }
+    mh[k] = m_run[k];
+    lh[k] = l;
   }
-  // Combine the two key parities.
 #pragma unroll
-  for (int h = 0; h < GQ; ++h) {
+  for (int h = 0; h < GQ; ++h)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       o[h][e].x += __shfl_xor_sync(0xffffffffu, o[h][e].x, 16);
       o[h][e].y += __shfl_xor_sync(0xffffffffu, o[h][e].y, 16);
     }
+  // With two warps per head, the second hands its state to the first
+  // through its (now idle) ring: o [GQ][128] then (m, l) [GQ][2].
+  float* hand = reinterpret_cast<float*>(my_ring);
+  if constexpr (kWarpsPerHead == 2) __syncthreads();
+  if (kWarpsPerHead == 2 && par == 1) {
     if (half == 0) {
-      const int hq = hk * GQ + h;
-      const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        *reinterpret_cast<float4*>(hand + h * kD + 4 * m) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+        *reinterpret_cast<float4*>(hand + h * kD + 64 + 4 * m) =
+            make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+      const int idx = k * 32 + lane;
+      if (idx < GQ * 8 && (idx & 7) == 0) {
+        hand[GQ * kD + 2 * (idx >> 3)] = mh[k];
+        hand[GQ * kD + 2 * (idx >> 3) + 1] = lh[k];
+      }
+    }
+  }
+  if constexpr (kWarpsPerHead == 2) __syncthreads();
+  if (par != 0) return;
+  const float* other = reinterpret_cast<const float*>(s_ring + (warp + p.Hkv) * kStages * kStageBytes);
+  const bool paired = kWarpsPerHead == 2;
+  // Merge state of head h: M = max(m0, m1), scales 2^(m0-M), 2^(m1-M).
+#pragma unroll
+  for (int h = 0; h < GQ; ++h) {
+    const float m1 = paired ? other[GQ * kD + 2 * h] : -INFINITY;
+    const float l1 = paired ? other[GQ * kD + 2 * h + 1] : 0.f;
+    // This warp's m and l of head h live in lanes 8h..8h+7 of iteration h / 4.
+    float m0 = 0.f, l0 = 0.f;
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+      const float mk = __shfl_sync(0xffffffffu, mh[k], (h * 8) & 31);
+      const float lk = __shfl_sync(0xffffffffu, lh[k], (h * 8) & 31);
+      if (k == (h * 8) / 32) {
+        m0 = mk;
+        l0 = lk;
+      }
+    }
+    const float M = fmaxf(m0, m1);
+    const float a0 = M == -INFINITY ? 0.f : exp2f(m0 - M);
+    const float a1 = M == -INFINITY ? 0.f : exp2f(m1 - M);
+    const int hq = hk * GQ + h;
+    const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
+    if (half == 0) {
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 b0 = paired ? *reinterpret_cast<const float4*>(other + h * kD + 4 * m) : zero4;
+      const float4 b1 = paired ? *reinterpret_cast<const float4*>(other + h * kD + 64 + 4 * m) : zero4;
       float* dst = p.part_o + slot * kD;
-      *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+      *reinterpret_cast<float4*>(dst + 4 * m) =
+          make_float4(a0 * o[h][0].x + a1 * b0.x, a0 * o[h][0].y + a1 * b0.y, a0 * o[h][1].x + a1 * b0.z,
+                      a0 * o[h][1].y + a1 * b0.w);
       *reinterpret_cast<float4*>(dst + 64 + 4 * m) =
-          make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
+          make_float4(a0 * o[h][2].x + a1 * b1.x, a0 * o[h][2].y + a1 * b1.y, a0 * o[h][3].x + a1 * b1.z,
+                      a0 * o[h][3].y + a1 * b1.w);
+    }
+    if (lane == 0) {
+      p.part_ml[slot * 2] = M;
+      p.part_ml[slot * 2 + 1] = a0 * l0 + a1 * l1;
     }
   }
 }
 
 // Merge the per-slice partials of one (batch, query head) with log-sum-exp
-// weights w_s = exp2(m_s - M): out = sum_s w_s o_s / sum_s w_s l_s.  Eight
-// warps split the slices; a lane owns four output elements.
+// weights: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max m_s.
+// One pass: each warp folds its slices (loaded four at a time, independent
+// loads) into a running (max, sum, vector); the eight warps combine in
+// shared memory.  A lane owns four output elements.
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                     int nsplit, int BH, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float s_w[kMaxSplits];
-  __shared__ float s_red[8];
+  __shared__ float s_m[8], s_l[8];
   __shared__ float4 s_acc[8][32];
   // The partials are written by the preceding grid.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float mx = -INFINITY;
-  for (int s = tid; s < nsplit; s += 256) mx = fmaxf(mx, part_ml[(static_cast<long long>(s) * BH + bh) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) s_red[warp] = mx;
-  __syncthreads();
-  float M = s_red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
-  __syncthreads();
-  float den = 0.f;
-  for (int s = tid; s < nsplit; s += 256) {
-    const long long slot = static_cast<long long>(s) * BH + bh;
-    const float w = exp2f(part_ml[slot * 2] - M);
-    s_w[s] = w;
-    den = fmaf(w, part_ml[slot * 2 + 1], den);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane == 0) s_red[warp] = den;
-  __syncthreads();
+  float M = -INFINITY, Lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s = warp; s < nsplit; s += 8) {
-    const float w = s_w[s];
-    const float4 v = *reinterpret_cast<const float4*>(part_o + (static_cast<long long>(s) * BH + bh) * kD + 4 * lane);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  for (int s0 = warp; s0 < nsplit; s0 += 32) {
+    float ms[4], ls[4];
+    float4 os[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int s = s0 + 8 * k;
+      if (s < nsplit) {
+        const long long slot = static_cast<long long>(s) * BH + bh;
+        ms[k] = part_ml[slot * 2];
+        ls[k] = part_ml[slot * 2 + 1];
+        os[k] = *reinterpret_cast<const float4*>(part_o + slot * kD + 4 * lane);
+      } else {
+        ms[k] = -INFINITY;
+        ls[k] = 0.f;
+        os[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float Mn = fmaxf(M, ms[k]);
+      if (Mn == -INFINITY) continue;
+      const float a = exp2f(M - Mn), w = exp2f(ms[k] - Mn);
+      Lsum = Lsum * a + ls[k] * w;
+      acc.x = acc.x * a + os[k].x * w;
+      acc.y = acc.y * a + os[k].y * w;
+      acc.z = acc.z * a + os[k].z * w;
+      acc.w = acc.w * a + os[k].w * w;
+      M = Mn;
+    }
   }
   s_acc[warp][lane] = acc;
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_l[warp] = Lsum;
+  }
   __syncthreads();
   if (warp == 0) {
+    float Mt = s_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) Mt = fmaxf(Mt, s_m[w]);
     float D = 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) D += s_red[w];
-    float4 t = s_acc[0][lane];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) {
-      t.x += s_acc[w][lane].x;
-      t.y += s_acc[w][lane].y;
-      t.z += s_acc[w][lane].z;
-      t.w += s_acc[w][lane].w;
+    for (int w = 0; w < 8; ++w) {
+      const float a = s_m[w] == -INFINITY ? 0.f : exp2f(s_m[w] - Mt);
+      D += a * s_l[w];
+      const float4 v = s_acc[w][lane];
+      t.x += a * v.x;
+      t.y += a * v.y;
+      t.z += a * v.z;
+      t.w += a * v.w;
     }
     const float inv = 1.f / D;
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + static_cast<long long>(bh) * kD + 4 * lane);
     dst[0] = __floats2bfloat162_rn(t.x * inv, t.y * inv);
     dst[1] = __floats2bfloat162_rn(t.z * inv, t.w * inv);
-    if (lse != nullptr && lane == 0) lse[bh] = (M + log2f(D)) * 0.69314718055994531f;
+    if (lse != nullptr && lane == 0) lse[bh] = (Mt + log2f(D)) * 0.69314718055994531f;
   }
 }
 
@@ -556,10 +607,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.freqs = a.freqs;
 
-  const int warps = std::max(a.Hkv, 1);
-  const size_t smem = static_cast<size_t>(2) * a.Hq * kD * sizeof(float) +
-                      static_cast<size_t>((kBlockKeys + 1) * 64 + 64 + 7 * 64) * sizeof(float2) +
-                      static_cast<size_t>(2) * kBlockKeys * 64 * sizeof(float) +
+  const int warps = kWarpsPerHead * a.Hkv;
+  const size_t smem = static_cast<size_t>(2) * a.Hq * kD * sizeof(float) +           // q
+                      static_cast<size_t>(2) * kBlockKeys * 64 * sizeof(float) +     // cos, sin
+                      static_cast<size_t>(8 + 9 + 1) * 64 * sizeof(float2) +         // R_-b, R_-8a, base
                       static_cast<size_t>(warps) * exchange_floats(GQ) * sizeof(float) +
                       static_cast<size_t>(warps) * kStages * kStageBytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
