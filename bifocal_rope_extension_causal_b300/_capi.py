@@ -63,6 +63,7 @@ SIGNATURES = {
     ]),
     "jl_bifocal_decode_noalloc_scratch_bytes": (_c.c_size_t, []),
     "jl_device_status": (_c.c_int, [_c.c_void_p]),
+    "jl_selftest_bounded_wait": (_c.c_int, [_c.c_longlong, _c.c_void_p]),
     "jl_last_error": (_c.c_char_p, []),
 }
 

@@ -187,6 +187,16 @@ size_t jl_bifocal_decode_noalloc_scratch_bytes(void);
  */
 int jl_device_status(void* cuda_stream);
 
+/*
+ * Exercises the failure path of jl_device_status without faulting the GPU:
+ * launches one thread that waits, with the library's bounded wait, on a
+ * barrier nothing arrives on.  After `limit_cycles` clock cycles (1 .. 4e9)
+ * the wait gives up, the status word is set and the kernel returns; the next
+ * jl_device_status on the stream then reports JL_ERR_TIMEOUT.  The paper has
+ * no counterpart: this is test support for the bounded waits.
+ */
+int jl_selftest_bounded_wait(long long limit_cycles, void* cuda_stream);
+
 /* Message of the last error on this thread ("" if none). Never NULL. */
 const char* jl_last_error(void);
 
