@@ -71,6 +71,16 @@ def test_small_shapes(jl, L, Hq, Hkv, d, wp, w0):
     full_check(jl, L, Hq, Hkv, d, wp, w0, 1e4, seed=L + 7 * w0)
 
 
+@pytest.mark.parametrize("L,Hq,Hkv,d,wp,w0", [
+    (5000, 16, 2, 128, 1700, 700),   # G = 3, GQA group 8, ragged, band across many tiles
+    (4096, 4, 2, 64, 2048, 1000),    # d = 64, G = 2, multi-tile straddles
+    (3000, 4, 1, 128, 800, 0),       # w0 = 0 over many tiles, G = 4
+    (2304, 8, 8, 128, 300, 2303),    # every pair local at G = 8
+])
+def test_mid_sizes(jl, L, Hq, Hkv, d, wp, w0):
+    full_check(jl, L, Hq, Hkv, d, wp, w0, 1e6, seed=L + w0)
+
+
 def test_batch_of_two(jl):
     full_check(jl, 150, 4, 2, 128, 40, 10, 1e6, seed=5, B=2)
 
