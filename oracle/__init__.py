@@ -20,4 +20,5 @@ from .bifocal import (  # noqa: F401
     bifocal_prefill,
     bifocal_prefill_three_pass,
     bifocal_decode,
+    bifocal_prefill_chunk,
 )

@@ -50,6 +50,9 @@ Pins (all in ``tests/``, ``-m "not gpu"``):
                      shift-invariant by multiples of G.
   bifocal_decode     decode at length L equals prefill row L-1 on an unrounded
                      cache; V == 1.
+  bifocal_prefill_chunk  with an unrounded cache equals the rows of
+                     bifocal_prefill (additive angle); a one-token chunk
+                     equals bifocal_decode on the same cache.
   bifocal_prefill_three_pass   agrees with bifocal_prefill (the two pin each
                      other: different algorithms for the same Eq. 1 result).
 """
@@ -61,6 +64,7 @@ import math
 import numpy as np
 
 __all__ = [
+    "bifocal_prefill_chunk",
     "group_size",
     "alias",
     "rope_frequencies",
@@ -292,6 +296,59 @@ def bifocal_prefill_three_pass(q, k, v, w0: int, w_pretrained: int, theta: float
             o_out[b, :, h, :] = (w_a[:, None] * o_a + w_b[:, None] * o_b
                                  - w_c[:, None] * o_c) / den[:, None]
             lse_out[b, h, :] = m + np.log(den)
+    return o_out, lse_out
+
+
+# --------------------------------------------------------------------------
+# Chunked prefill against a cache  [D, Method: "KV cache invariant"]
+# --------------------------------------------------------------------------
+
+def bifocal_prefill_chunk(q, k, v, k_cache, P0: int, w0: int, w_pretrained: int, theta: float,
+                          scale: float | None = None, round_rotated_qk: bool = False):
+    """Queries of a chunk at positions P0 .. P0+C-1 against a cache of
+    positions 0 .. P0-1 plus the chunk's own keys (causal).
+
+    q: [B, C, Hq, d] raw chunk queries; k: [B, C, Hkv, d] raw chunk keys;
+    v: [B, P0+C, Hkv, d] values of every position; k_cache: [B, >= P0, Hkv, d]
+    holding R_j x_j for j < P0 as stored (read exactly, never modified).
+    G = group_size(P0 + C, w_pretrained).  Cached keys take their aliased
+    rotation through the correction R_{f(j) - j} applied to the stored key,
+    the chunk's keys are rotated from raw; then the same piecewise score and
+    masked causal softmax as bifocal_prefill.  ``round_rotated_qk`` rounds
+    every rotated query and key that is not already a stored cache entry to
+    bf16 (the tensor-core operands).  Returns (o [B, C, Hq, d], lse [B, Hq, C]).
+    """
+    B, C, Hq, d = q.shape
+    Hkv = k.shape[2]
+    group = Hq // Hkv
+    Lt = P0 + C
+    G = group_size(Lt, w_pretrained)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rnd = round_to_bf16 if round_rotated_qk else (lambda a: a)
+    qpos = np.arange(P0, Lt, dtype=np.int64)
+    kpos = np.arange(Lt, dtype=np.int64)
+    cpos = np.arange(P0, dtype=np.int64)
+    o_out = np.zeros((B, C, Hq, d))
+    lse_out = np.zeros((B, Hq, C))
+    dist = qpos[:, None] - kpos[None, :]
+    for b in range(B):
+        for hk in range(Hkv):
+            cached = np.asarray(k_cache[b, :P0, hk, :], dtype=np.float64)
+            xk = np.asarray(k[b, :, hk, :], dtype=np.float64)
+            k_abs = np.concatenate([cached, rnd(rope_rotate(xk, qpos, theta))], axis=0)
+            k_rem = np.concatenate([rnd(rope_rotate(cached, alias(cpos, G) - cpos, theta)),
+                                    rnd(rope_rotate(xk, alias(qpos, G), theta))], axis=0)
+            vk = np.asarray(v[b, :Lt, hk, :], dtype=np.float64)
+            for h in range(hk * group, (hk + 1) * group):
+                xq = np.asarray(q[b, :, h, :], dtype=np.float64)
+                q_abs = rnd(rope_rotate(xq, qpos, theta))
+                q_rem = rnd(rope_rotate(xq, alias(qpos, G), theta))
+                s = scale * np.where(dist <= w0, q_abs @ k_abs.T, q_rem @ k_rem.T)
+                s = np.where(dist < 0, -np.inf, s)
+                o, lse = _softmax_rows(s, vk)
+                o_out[b, :, h, :] = o
+                lse_out[b, h, :] = lse
     return o_out, lse_out
 
 

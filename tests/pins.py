@@ -292,6 +292,36 @@ def pin_sampled_rows(orc):
         assert np.abs(ls_[0, h] - lse[0, h, rows[h]]).max() <= 1e-14
 
 
+def pin_chunk_equals_prefill_rows(orc):
+    """A chunk against an unrounded cache (R_j x_j in fp64) equals the rows of
+    a prefill over all positions so far (same G): the correction rotation
+    R_{f(j)-j} R_j = R_{f(j)} (additive angle, "KV cache invariant")."""
+    L, Hq, Hkv, d, wp, w0, theta = 60, 4, 2, 16, 17, 5, 1e4
+    q, k, v = _rand((1, L, Hq, d), 51), _rand((1, L, Hkv, d), 52), _rand((1, L, Hkv, d), 53)
+    for P0, C in ((0, 60), (20, 40), (33, 1), (59, 1), (1, 59)):
+        Lt = P0 + C
+        cache = orc.rope_rotate(k[0, :P0], np.arange(P0), theta)[None] if P0 else np.zeros((1, 0, Hkv, d))
+        oc, lc = orc.bifocal_prefill_chunk(q[:, P0:Lt], k[:, P0:Lt], v, cache, P0, w0, wp, theta)
+        op, lp = orc.bifocal_prefill(q[:, :Lt], k[:, :Lt], v[:, :Lt], w0, wp, theta)
+        assert np.abs(oc - op[:, P0:Lt]).max() <= 1e-12, (P0, C)
+        assert np.abs(lc - lp[:, :, P0:Lt]).max() <= 1e-12, (P0, C)
+
+
+def pin_one_token_chunk_is_decode(orc):
+    """A one-token chunk against a stored (bf16-rounded) cache equals decode
+    on the same cache with the token's own rotated key appended."""
+    L, Hq, Hkv, d, wp, w0, theta = 45, 4, 1, 16, 10, 3, 1e4
+    q, k, v = _rand((1, L, Hq, d), 61), _rand((1, L, Hkv, d), 62), _rand((1, L, Hkv, d), 63)
+    cache = orc.round_to_bf16(orc.rope_rotate(k[0], np.arange(L), theta))[None]
+    P0 = L - 1
+    oc, lc = orc.bifocal_prefill_chunk(q[:, P0:], k[:, P0:], v, cache, P0, w0, wp, theta)
+    full_cache = cache.copy()
+    full_cache[0, P0] = orc.rope_rotate(k[0, P0:], [P0], theta)[0]
+    od, ld = orc.bifocal_decode(q[:, P0], full_cache, v, L, w0, wp, theta)
+    assert np.abs(oc[:, 0] - od).max() <= 1e-12
+    assert np.abs(lc[:, :, 0] - ld).max() <= 1e-12
+
+
 ALL_PINS = [
     pin_group_size_bruteforce,
     pin_alias_floor,
@@ -307,4 +337,6 @@ ALL_PINS = [
     pin_values_one,
     pin_remote_shift_invariance,
     pin_sampled_rows,
+    pin_chunk_equals_prefill_rows,
+    pin_one_token_chunk_is_decode,
 ]

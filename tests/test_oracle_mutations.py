@@ -38,6 +38,10 @@ MUTATIONS = [
     ("angle composition bit test", "bit = ((mag >> j) & 1)", "bit = ((mag >> (j + 1)) & 1)"),
     ("three-pass sign", "- w_c[:, None] * o_c", "+ w_c[:, None] * o_c"),
     ("bf16 rounding keeps 7 bits", "quantum = np.ldexp(1.0, e - 8)", "quantum = np.ldexp(1.0, e - 7)"),
+    ("chunk: cached keys not corrected", "rnd(rope_rotate(cached, alias(cpos, G) - cpos, theta))",
+     "rnd(cached)"),
+    ("chunk: query positions from zero", "qpos = np.arange(P0, Lt, dtype=np.int64)",
+     "qpos = np.arange(0, C, dtype=np.int64)"),
 ]
 
 
