@@ -442,6 +442,55 @@ def run_profile_decode(args):
     return 0
 
 
+def run_profile_chunked(args):
+    """Chunked prefill of one sequence: every chunk attends to the cache
+    filled by the chunks before it.  Reports the per-chunk times and the
+    causal-pair TFLOP/s of the whole sequence."""
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    w = PREFILL
+    L, C = (int(x) for x in args.profile_chunked)
+    dev = torch.device("cuda", 0)
+    q, k, v = synth.prefill_inputs(L, w.Hq, w.Hkv, w.d, w.index)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    kc = torch.empty((1, L, w.Hkv, w.d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    ws = jl.alloc_workspace(max(jl.load().jl_bifocal_prefill_chunk_workspace_size(1, C, P0, w.Hq, w.Hkv, w.d,
+                                                                                   w.w_pretrained)
+                                for P0 in range(0, L, C)), dev)
+    starts = list(range(0, L, C))
+    outs = [(torch.empty((1, min(C, L - s), w.Hq, w.d), dtype=torch.bfloat16, device=dev),
+             torch.empty((1, w.Hq, min(C, L - s)), dtype=torch.float32, device=dev)) for s in starts]
+
+    def sweep(events=None):
+        for i, s0 in enumerate(starts):
+            e = min(L, s0 + C)
+            if events:
+                events[i].record()
+            jl.prefill_chunk(qd[:, s0:e], kd[:, s0:e], vd[:, s0:e], kc, vc, s0, w.w0, w.w_pretrained, w.theta,
+                             out=outs[i][0], lse=outs[i][1], workspace=ws)
+        if events:
+            events[-1].record()
+
+    for _ in range(args.warmup):
+        sweep()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(starts) + 1)]
+        sweep(ev)
+        torch.cuda.synchronize()
+        times.append([ev[i].elapsed_time(ev[i + 1]) for i in range(len(starts))])
+    jl.device_status()
+    per_chunk = [min(t[i] for t in times) for i in range(len(starts))]
+    total = sum(per_chunk)
+    flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
+    print(json.dumps({"profile_chunked_L": L, "C": C, "chunk_ms": [round(x, 3) for x in per_chunk],
+                      "total_ms": total, "tflops": flops / (total * 1e-3) / 1e12,
+                      "G_per_chunk": [jl.group_size(min(L, s + C), w.w_pretrained) for s in starts]}))
+    return 0
+
+
 def load_traffic():
     """DRAM bytes per attention launch from the committed ncu capture
     (profiles/prefill_attention_traffic.json), or None if the kernel sources
@@ -469,6 +518,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="L",
                     help="profiling mode: only decode steps of the decode workload at cache length L")
+    ap.add_argument("--profile-chunked", type=int, nargs=2, default=None, metavar=("L", "C"),
+                    help="measurement mode: the 4x-extension head layout prefilled in chunks of C "
+                         "tokens up to L against the cache (one G per chunk from its total length)")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                     help="profiling mode: only the prefill of the 4x-extension head layout at "
                          "sequence length L (G from L), warm-up + steps calls; prints timings")
@@ -480,6 +532,8 @@ def main():
         return run_profile_prefill(args)
     if args.profile_decode:
         return run_profile_decode(args)
+    if args.profile_chunked:
+        return run_profile_chunked(args)
     return run_ours(args)
 
 

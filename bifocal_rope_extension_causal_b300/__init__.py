@@ -18,6 +18,7 @@ __all__ = [
     "prefill_workspace_size",
     "decode_workspace_size",
     "prefill",
+    "prefill_chunk",
     "decode",
     "device_status",
     "JetLongError",
@@ -90,6 +91,32 @@ def prefill(q, k, v, w0: int, w_pretrained: int, rope_theta: float, softmax_scal
     check(load().jl_bifocal_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq, Hkv, d, int(w0),
         int(w_pretrained), float(rope_theta), float(softmax_scale), _ptr(k_rot_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def prefill_chunk(q, k, v, k_cache, v_cache, P0: int, w0: int, w_pretrained: int,
+                  rope_theta: float, softmax_scale: float = 0.0, *, out=None, lse=None,
+                  want_lse: bool = True, workspace=None, stream=None):
+    """Chunked prefill: q [B, C, Hq, d], k/v [B, C, Hkv, d] raw chunk tokens at
+    positions P0 .. P0+C-1; k_cache/v_cache [B, Lcap, Hkv, d] hold positions
+    0 .. P0-1 and receive the chunk.  Returns (o [B, C, Hq, d], lse [B, Hq, C])."""
+    torch = _torch()
+    for name, t, nd in (("q", q, 4), ("k", k, 4), ("v", v, 4), ("k_cache", k_cache, 4),
+                        ("v_cache", v_cache, 4)):
+        _need_cuda_bf16(name, t, nd)
+    B, C, Hq, d = q.shape
+    Hkv, Lcap = k.shape[2], k_cache.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, C), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(load().jl_bifocal_prefill_chunk_workspace_size(
+            B, C, int(P0), Hq, Hkv, d, int(w_pretrained)), q.device)
+    check(load().jl_bifocal_prefill_chunk(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), int(P0), Lcap, _ptr(out), _ptr(lse),
+        B, C, Hq, Hkv, d, int(w0), int(w_pretrained), float(rope_theta), float(softmax_scale),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, lse
 

@@ -46,6 +46,15 @@ SIGNATURES = {
         _c.c_int, _c.c_int, _c.c_float,                    # w0, w_pretrained, softmax_scale
         _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
     ]),
+    "jl_bifocal_prefill_chunk_workspace_size": (_c.c_size_t, [_c.c_int] * 7),
+    "jl_bifocal_prefill_chunk": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k, v (chunk, raw)
+        _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int,      # k_cache, v_cache, P0, Lcap
+        _c.c_void_p, _c.c_void_p,                          # o, lse
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,  # B, C, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_double, _c.c_float,       # w0, w_pretrained, theta, scale
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_bifocal_decode_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
     "jl_bifocal_decode": (_c.c_int, [
         _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k_cache, v_cache

@@ -1,6 +1,7 @@
 // C ABI of libjetlong.so (declared in include/jetlong.h): argument
 // validation, workspace carving, and the launches of the CUDA path.  The
 // library allocates no device memory; every buffer is the caller's.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdarg.h>
@@ -132,9 +133,13 @@ int jl_bifocal_rope(const void* q, const void* k, int B, int L, int Hq, int Hkv,
   const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, bif);
   auto stream = static_cast<cudaStream_t>(cuda_stream);
   const RopeFreqs fr = make_rope_freqs(d, rope_theta);
-  cudaError_t e = launch_rope_prepass(q, B, L, Hq, d, G, fr, w.qa, bif ? w.qr : nullptr, nullptr, stream);
+  const TensorView none{nullptr, 0, 0, 0, 0};
+  cudaError_t e = launch_rope_prepass(q, B, L, Hq, d, G, 0, fr, head_major(w.qa, Hq, L, d),
+                                      bif ? head_major(w.qr, Hq, L, d) : none, none, stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (Q)");
-  e = launch_rope_prepass(k, B, L, Hkv, d, G, fr, w.ka, bif ? w.kr : nullptr, k_rot_out, stream);
+  e = launch_rope_prepass(k, B, L, Hkv, d, G, 0, fr, head_major(w.ka, Hkv, L, d),
+                          bif ? head_major(w.kr, Hkv, L, d) : none,
+                          k_rot_out ? cache_layout(k_rot_out, L, Hkv, d, L) : none, stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (K)");
   return JL_OK;
 }
@@ -154,8 +159,13 @@ int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int H
   const int G = static_cast<int>(jl::group_size(L, w_pretrained));
   const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, G > 1);
   PrefillArgs a;
-  a.qa = w.qa; a.qr = w.qr; a.ka = w.ka; a.kr = w.kr; a.v = v; a.o = o; a.lse = lse;
-  a.B = B; a.L = L; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
+  a.qa = head_major(w.qa, Hq, L, d);
+  a.qr = head_major(w.qr, Hq, L, d);
+  a.ka = head_major(w.ka, Hkv, L, d);
+  a.kr = head_major(w.kr, Hkv, L, d);
+  a.v = cache_layout(v, L, Hkv, d, L);
+  a.o = o; a.lse = lse;
+  a.B = B; a.Lq = L; a.Lk = L; a.q_base = 0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
   const cudaError_t e = launch_prefill_attention(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention: kernel launch");
@@ -177,6 +187,86 @@ int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, flo
   if (rc != JL_OK) return rc;
   return jl_bifocal_attention(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, softmax_scale,
                               workspace, workspace_bytes, cuda_stream);
+}
+
+size_t jl_bifocal_prefill_chunk_workspace_size(int B, int C, int P0, int Hq, int Hkv, int d,
+                                               int w_pretrained) {
+  if (B < 1 || C < 1 || P0 < 0 || Hq < 1 || Hkv < 1 || d < 1 || w_pretrained < 1) return 0;
+  const int Lk = P0 + C;
+  const bool bif = jl::group_size(Lk, w_pretrained) > 1;
+  const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * C * d * 2);
+  const size_t krbytes = align_up(static_cast<size_t>(B) * Hkv * Lk * d * 2);
+  return (bif ? 2 : 1) * qbytes + (bif ? krbytes : 0);
+}
+
+int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+                             int P0, int Lcap, void* o, float* lse, int B, int C, int Hq, int Hkv, int d,
+                             int w0, int w_pretrained, double rope_theta, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q || !k || !v || !k_cache || !v_cache || !o)
+    return fail(JL_ERR_INVALID, "prefill_chunk: null q/k/v/cache/o pointer");
+  if (C < 1 || P0 < 0) return fail(JL_ERR_INVALID, "prefill_chunk: need C >= 1 and P0 >= 0");
+  if (static_cast<long long>(P0) + C > Lcap)
+    return fail(JL_ERR_INVALID, "prefill_chunk: P0 + C = %lld exceeds Lcap = %d", static_cast<long long>(P0) + C, Lcap);
+  int rc = check_prefill_shape("prefill_chunk", B, C, Hq, Hkv, d, w0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta))
+    return fail(JL_ERR_INVALID, "prefill_chunk: rope_theta must be > 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(o) || (lse && !aligned16(lse)))
+    return fail(JL_ERR_INVALID, "prefill_chunk: every pointer must be 16-byte aligned");
+  rc = check_workspace("prefill_chunk", workspace, workspace_bytes,
+                       jl_bifocal_prefill_chunk_workspace_size(B, C, P0, Hq, Hkv, d, w_pretrained));
+  if (rc != JL_OK) return rc;
+  const int Lk = P0 + C;
+  const int G = static_cast<int>(jl::group_size(Lk, w_pretrained));
+  const bool bif = G > 1;
+  auto* ws = static_cast<unsigned char*>(workspace);
+  const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * C * d * 2);
+  void* qa = ws;
+  void* qr = bif ? ws + qbytes : qa;
+  void* kr = bif ? ws + 2 * qbytes : nullptr;
+  auto stream = static_cast<cudaStream_t>(cuda_stream);
+  const RopeFreqs fr = make_rope_freqs(d, rope_theta);
+  const TensorView none{nullptr, 0, 0, 0, 0};
+  const size_t row_elems = static_cast<size_t>(Hkv) * d;
+  auto* kc = static_cast<__nv_bfloat16_raw*>(k_cache);
+  // 1. Queries at positions P0 .. P0+C-1, both rotations.
+  cudaError_t e = launch_rope_prepass(q, B, C, Hq, d, G, P0, fr, head_major(qa, Hq, C, d),
+                                      bif ? head_major(qr, Hq, C, d) : none, none, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: pre-pass (Q)");
+  // 2. New keys: absolute rotation appended to the cache, aliased rotation
+  //    into rows P0.. of K_rem.
+  TensorView kr_all = bif ? head_major(kr, Hkv, Lk, d) : none;
+  TensorView kr_new = kr_all;
+  if (bif) kr_new.base = static_cast<const unsigned char*>(kr) + static_cast<size_t>(P0) * d * 2;
+  TensorView kc_new = cache_layout(kc + static_cast<size_t>(P0) * row_elems, Lcap, Hkv, d, C);
+  e = launch_rope_prepass(k, B, C, Hkv, d, G, P0, fr, none, kr_new, kc_new, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: pre-pass (K)");
+  // 3. Cached keys 0 .. P0-1: aliased rotation by the correction R_{f(k)-k}.
+  if (bif && P0 > 0) {
+    e = launch_rope_correct(k_cache, B, P0, Lcap, Hkv, d, G, fr, kr_all, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: correction pass");
+  }
+  // 4. New values appended to the value cache.
+  e = cudaMemcpy2DAsync(static_cast<unsigned char*>(v_cache) + static_cast<size_t>(P0) * row_elems * 2,
+                        static_cast<size_t>(Lcap) * row_elems * 2, v, static_cast<size_t>(C) * row_elems * 2,
+                        static_cast<size_t>(C) * row_elems * 2, B, cudaMemcpyDeviceToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: value append");
+  // 5. Attention of the C query rows over keys 0 .. P0+C-1.
+  PrefillArgs a;
+  a.qa = head_major(qa, Hq, C, d);
+  a.qr = head_major(qr, Hq, C, d);
+  a.ka = cache_layout(k_cache, Lcap, Hkv, d, Lk);
+  a.kr = bif ? kr_all : a.ka;
+  a.v = cache_layout(v_cache, Lcap, Hkv, d, Lk);
+  a.o = o; a.lse = lse;
+  a.B = B; a.Lq = C; a.Lk = Lk; a.q_base = P0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
+  a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+  e = launch_prefill_attention(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: attention kernel");
+  return JL_OK;
 }
 
 size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap) {

@@ -16,26 +16,48 @@ struct RopeFreqs {
 };
 RopeFreqs make_rope_freqs(int d, double theta);
 
-// ---- RoPE pre-pass (rope_prepass.cu) ---------------------------------------
-// Rotates x [B, L, H, d] (raw) at absolute positions into out_abs [B, H, L, d]
-// and, if out_rem != nullptr, at aliased positions f(p) = p / G into out_rem
-// [B, H, L, d]; if out_cache != nullptr also writes the absolute rotation in
-// the input layout [B, L, H, d].
-cudaError_t launch_rope_prepass(const void* x, int B, int L, int H, int d, int G,
-                                const RopeFreqs& freqs, void* out_abs, void* out_rem,
-                                void* out_cache, cudaStream_t stream);
+// A bf16 tensor addressed as [B, H, rows, d]: element (b, h, row, e) lives at
+// base + b * sb + h * sh + row * sr + e (strides in elements).  Head-major
+// workspace tensors [B, H, L, d] and cache-layout tensors [B, Lcap, H, d]
+// are both described this way.
+struct TensorView {
+  const void* base;
+  long long sb, sh, sr;
+  int rows;
+};
+inline TensorView head_major(const void* base, int H, int L, int d) {
+  return {base, static_cast<long long>(H) * L * d, static_cast<long long>(L) * d, d, L};
+}
+inline TensorView cache_layout(const void* base, int Lcap, int H, int d, int rows) {
+  return {base, static_cast<long long>(Lcap) * H * d, d, static_cast<long long>(H) * d, rows};
+}
 
-// ---- Prefill attention over pre-rotated operands (prefill_*.cu) -------------
+// ---- RoPE pre-pass (rope_prepass.cu) ---------------------------------------
+// Rotates x [B, C, H, d] (raw; row p is position pos0 + p) at the absolute
+// positions into `abs` and at the aliased positions f(pos) = pos / G into
+// `rem`, also writing the absolute rotation into `cache` (rows p of each
+// view; a view with a null base is skipped).
+cudaError_t launch_rope_prepass(const void* x, int B, int C, int H, int d, int G, int pos0,
+                                const RopeFreqs& freqs, TensorView abs, TensorView rem,
+                                TensorView cache, cudaStream_t stream);
+
+// Turns keys already rotated at their absolute positions k (cache [B, Lcap,
+// H, d], rows 0 .. P0-1) into keys rotated at f(k) = k / G by the
+// correction rotation R_{f(k) - k}; writes rows 0 .. P0-1 of `rem`.
+cudaError_t launch_rope_correct(const void* k_cache, int B, int P0, int Lcap, int H, int d, int G,
+                                const RopeFreqs& freqs, TensorView rem, cudaStream_t stream);
+
+// ---- Prefill attention over pre-rotated operands (prefill_tc.cu) -------------
+// Query rows 0 .. Lq-1 sit at positions q_base .. q_base+Lq-1 and attend
+// causally to keys 0 .. q_base+row (Lk = q_base + Lq key rows).
 struct PrefillArgs {
-  const void* qa;  // bf16 [B, Hq, L, d]  R_q x_q
-  const void* qr;  // bf16 [B, Hq, L, d]  R_f(q) x_q   (== qa when G == 1)
-  const void* ka;  // bf16 [B, Hkv, L, d] R_k x_k
-  const void* kr;  // bf16 [B, Hkv, L, d] R_f(k) x_k  (== ka when G == 1)
-  const void* v;   // bf16 [B, L, Hkv, d]
-  void* o;         // bf16 [B, L, Hq, d]
-  float* lse;      // fp32 [B, Hq, L] or nullptr
-  int B, L, Hq, Hkv, d, w0, G;
-  float scale_log2;  // softmax scale * log2(e)
+  TensorView qa, qr;  // R_q x_q and R_f(q) x_q (qr == qa when G == 1); rows = Lq
+  TensorView ka, kr;  // R_k x_k and R_f(k) x_k (kr == ka when G == 1); rows = Lk
+  TensorView v;       // values; rows = Lk
+  void* o;            // bf16 [B, Lq, Hq, d]
+  float* lse;         // fp32 [B, Hq, Lq] or nullptr
+  int B, Lq, Lk, q_base, Hq, Hkv, d, w0, G;
+  float scale_log2;   // softmax scale * log2(e)
 };
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 

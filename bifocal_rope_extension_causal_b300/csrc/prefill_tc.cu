@@ -66,7 +66,7 @@ struct Cfg {
 };
 
 struct TcParams {
-  int B, L, Hq, Hkv, w0, G, npairs;
+  int B, Lq, q_base, Hq, Hkv, w0, G, npairs;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -79,9 +79,11 @@ struct Plan {
   int nr, jl0, jmax, nv;
 };
 
-__device__ __forceinline__ Plan make_plan(int q0, int L, int w0) {
+// q0: position of the CTA's first query row; qend: one past the last query
+// position of the call.
+__device__ __forceinline__ Plan make_plan(int q0, int qend, int w0) {
   Plan p;
-  const int qlast = min(q0 + 2 * kBM - 1, L - 1);
+  const int qlast = min(q0 + 2 * kBM - 1, qend - 1);
   p.jmax = qlast / kBN;
   const int t = qlast - w0 - 1;  // remote pairs with key tile j iff kBN * j <= t
   p.nr = t >= 0 ? min(t / kBN, p.jmax) + 1 : 0;
@@ -125,8 +127,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
   const int bh = u % BH;
   const int b = bh / prm.Hq, h = bh % prm.Hq;
   const int hk = h / (prm.Hq / prm.Hkv);
-  const int q0 = pair * 2 * kBM;
-  const Plan plan = make_plan(q0, prm.L, prm.w0);
+  const int row0 = pair * 2 * kBM;        // first query row of the CTA (local)
+  const int q0 = prm.q_base + row0;       // its position
+  const Plan plan = make_plan(q0, prm.q_base + prm.Lq, prm.w0);
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -170,12 +173,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int qz = b * prm.Hq + h, kz = b * prm.Hkv + hk;
       auto load_q = [&](const CUtensorMap* m) {
         mbar_arrive_expect_tx(bar(bars.q_full), 2 * kTileBytes);
         for (int t = 0; t < 2; ++t)
           for (int c = 0; c < kBoxes; ++c)
-            tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, m, bar(bars.q_full), 64 * c, q0 + t * kBM, qz);
+            tma_load_4d(sQ + t * kTileBytes + c * kBoxBytes, m, bar(bars.q_full), 64 * c, h, row0 + t * kBM, b);
       };
       load_q(plan.nr > 0 ? &tm_qr : &tm_qa);
       bool ok = true;
@@ -197,10 +199,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
           const uint32_t dst = sRing + s * kTileBytes;
           mbar_arrive_expect_tx(bar(bars.full[s]), kTileBytes);
           for (int c = 0; c < kBoxes; ++c) {
-            if (part == 0)
-              tma_load_3d(dst + c * kBoxBytes, remote ? &tm_kr : &tm_ka, bar(bars.full[s]), 64 * c, j * kBN, kz);
-            else
-              tma_load_4d(dst + c * kBoxBytes, &tm_v, bar(bars.full[s]), 64 * c, hk, j * kBN, b);
+            tma_load_4d(dst + c * kBoxBytes, part == 0 ? (remote ? &tm_kr : &tm_ka) : &tm_v, bar(bars.full[s]),
+                        64 * c, hk, j * kBN, b);
           }
         }
       }
@@ -269,7 +269,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
     // ------------------------------------------------------------ softmax warps
     const int t = warp >> 2;           // query tile
     const int r = (warp & 3) * 32 + lane;  // row in tile = TMEM lane
-    const int q = q0 + t * kBM + r;
+    const int q = q0 + t * kBM + r;        // query position
+    const int qrow = row0 + t * kBM + r;   // output row
     const int q0t = q0 + t * kBM;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
@@ -374,13 +375,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
     if (ok && mbar_wait(bar(bars.pv_done[t]), (plan.nv - 1) & 1, &s_abort, kWaitLimit)) {
       tc_fence_after();
       const float inv = 1.f / l_run;
-      __nv_bfloat16* orow = prm.o + ((static_cast<long long>(b) * prm.L + q) * prm.Hq + h) * D;
+      __nv_bfloat16* orow = prm.o + ((static_cast<long long>(b) * prm.Lq + qrow) * prm.Hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait(o);
-        if (q < prm.L) {
+        if (qrow < prm.Lq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -393,8 +394,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
           }
         }
       }
-      if (q < prm.L && prm.lse != nullptr)
-        prm.lse[(static_cast<long long>(b) * prm.Hq + h) * prm.L + q] =
+      if (qrow < prm.Lq && prm.lse != nullptr)
+        prm.lse[(static_cast<long long>(b) * prm.Hq + h) * prm.Lq + qrow] =
             (m_used + log2f(l_run)) * 0.69314718055994531f;
     } else if (ok) {
       fail(10);
@@ -409,42 +410,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
   }
 }
 
+// 4-D map (d, head, row, batch) over a TensorView, boxes of 64 columns x
+// `rows` rows of one head.
+bool make_view_map(CUtensorMap* m, const TensorView& t, int d, int heads, int B, int rows) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(heads),
+                            static_cast<uint64_t>(t.rows), static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(t.sh) * 2, static_cast<uint64_t>(t.sr) * 2,
+                               static_cast<uint64_t>(t.sb) * 2};
+  const uint32_t box[4] = {64, 1, static_cast<uint32_t>(rows), 1};
+  return make_tmap_bf16(m, t.base, 4, dims, strides, box, true);
+}
+
 template <int D>
 cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
   CUtensorMap tqa, tqr, tka, tkr, tv;
-  const uint32_t box3[3] = {64, kBM, 1};
-  {
-    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.L),
-                              static_cast<uint64_t>(a.B) * a.Hq};
-    const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(a.L) * D * 2ull};
-    if (!make_tmap_bf16(&tqa, a.qa, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&tqr, a.qr, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.L),
-                              static_cast<uint64_t>(a.B) * a.Hkv};
-    const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(a.L) * D * 2ull};
-    if (!make_tmap_bf16(&tka, a.ka, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&tkr, a.kr, 3, dims, strides, box3, true)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv),
-                              static_cast<uint64_t>(a.L), static_cast<uint64_t>(a.B)};
-    const uint64_t strides[3] = {D * 2ull, static_cast<uint64_t>(a.Hkv) * D * 2ull,
-                                 static_cast<uint64_t>(a.L) * a.Hkv * D * 2ull};
-    const uint32_t box4[4] = {64, 1, kBN, 1};
-    if (!make_tmap_bf16(&tv, a.v, 4, dims, strides, box4, true)) return cudaErrorInvalidValue;
-  }
+  if (!make_view_map(&tqa, a.qa, D, a.Hq, a.B, kBM) || !make_view_map(&tqr, a.qr, D, a.Hq, a.B, kBM) ||
+      !make_view_map(&tka, a.ka, D, a.Hkv, a.B, kBN) || !make_view_map(&tkr, a.kr, D, a.Hkv, a.B, kBN) ||
+      !make_view_map(&tv, a.v, D, a.Hkv, a.B, kBN))
+    return cudaErrorInvalidValue;
   TcParams p;
   p.B = a.B;
-  p.L = a.L;
+  p.Lq = a.Lq;
+  p.q_base = a.q_base;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   // One G for the call; with G == 1 both rotations coincide, so every pair
   // is scored in the local phase (no window).
-  p.w0 = (a.G == 1 || a.w0 >= a.L) ? (1 << 30) : a.w0;
+  p.w0 = (a.G == 1 || a.w0 >= a.Lk) ? (1 << 30) : a.w0;
   p.G = a.G;
-  p.npairs = (a.L + 2 * kBM - 1) / (2 * kBM);
+  p.npairs = (a.Lq + 2 * kBM - 1) / (2 * kBM);
   p.scale_log2 = a.scale_log2;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
@@ -453,6 +447,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = static_cast<long long>(p.npairs) * a.B * a.Hq;
+  if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   prefill_tc_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(tqa, tqr, tka, tkr, tv, p);
   return cudaGetLastError();

@@ -116,6 +116,43 @@ int jl_bifocal_attention(const void* v, void* o, float* lse,
                          void* cuda_stream);
 
 /*
+ * Chunked prefill against an absolute-position KV cache: the prompt arrives
+ * in chunks, and each chunk attends to everything before it through the
+ * cache that earlier calls filled (this entry point, jl_bifocal_prefill's
+ * k_rot_out, or decode-side appends).
+ *
+ * The cache holds positions [0, P0): keys rotated at their absolute
+ * positions, R_k x_k, and values.  The chunk is C raw tokens at positions
+ * [P0, P0 + C).  With G = jl_group_size(P0 + C, w_pretrained) (one G for the
+ * call, from the total length after the chunk), query p in the chunk attends
+ * to keys 0 .. p with the bifocal score; cached keys reach their aliased
+ * rotation through the correction R_{f(k)-k} (digest page, "KV cache
+ * invariant") -- positions [0, P0) of the cache are only read.  The chunk's
+ * rotated keys and its values are appended to the cache at [P0, P0 + C).
+ * The result equals rows [P0, P0 + C) of a jl_bifocal_prefill over the first
+ * P0 + C tokens when both see the same G.
+ *
+ *  q        bf16 [B, C, Hq, d]   raw chunk queries
+ *  k, v     bf16 [B, C, Hkv, d]  raw chunk keys, values
+ *  k_cache  bf16 [B, Lcap, Hkv, d]  rows [0, P0) read, rows [P0, P0+C) written
+ *  v_cache  bf16 [B, Lcap, Hkv, d]  same
+ *  P0 >= 0, C >= 1, P0 + C <= Lcap
+ *  o        bf16 [B, C, Hq, d];  lse fp32 [B, Hq, C] (may be NULL)
+ *  workspace >= jl_bifocal_prefill_chunk_workspace_size(...) bytes
+ */
+size_t jl_bifocal_prefill_chunk_workspace_size(int B, int C, int P0, int Hq, int Hkv, int d,
+                                               int w_pretrained);
+
+int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v,
+                             void* k_cache, void* v_cache, int P0, int Lcap,
+                             void* o, float* lse,
+                             int B, int C, int Hq, int Hkv, int d,
+                             int w0, int w_pretrained, double rope_theta,
+                             float softmax_scale,
+                             void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+
+/*
  * Bytes of device workspace jl_bifocal_decode needs (per-split partial
  * softmax statistics and outputs) for caches of up to Lcap positions.
  * Returns 0 for invalid sizes.
