@@ -20,6 +20,7 @@ __all__ = [
     "prefill",
     "prefill_chunk",
     "decode",
+    "decode_varlen",
     "device_status",
     "JetLongError",
 ]
@@ -142,6 +143,36 @@ def decode(q, k_cache, v_cache, L: int, w0: int, w_pretrained: int, rope_theta: 
     check(load().jl_bifocal_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), int(L), Lcap, _ptr(out), _ptr(lse), B, Hq, Hkv, d,
         int(w0), int(w_pretrained), float(rope_theta), float(softmax_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def decode_varlen(q, k_cache, v_cache, seqlens, w0: int, w_pretrained: int, rope_theta: float,
+                  softmax_scale: float = 0.0, *, max_len=None, out=None, lse=None, want_lse: bool = True,
+                  workspace=None, stream=None):
+    """Batched decode, one length per sequence.  seqlens: int32 CUDA tensor [B]
+    (sequence b's new token is at position seqlens[b] - 1).  Returns
+    (o [B, Hq, d], lse [B, Hq])."""
+    torch = _torch()
+    _need_cuda_bf16("q", q, 3)
+    _need_cuda_bf16("k_cache", k_cache, 4)
+    _need_cuda_bf16("v_cache", v_cache, 4)
+    if not (isinstance(seqlens, torch.Tensor) and seqlens.is_cuda and seqlens.dtype == torch.int32
+            and seqlens.dim() == 1 and seqlens.is_contiguous()):
+        raise TypeError("seqlens must be a contiguous 1-d int32 CUDA tensor")
+    B, Hq, d = q.shape
+    Lcap, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if max_len is None:
+        max_len = int(seqlens.max().item())
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(decode_workspace_size(B, Hq, d, Lcap), q.device)
+    check(load().jl_bifocal_decode_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), int(max_len), Lcap, _ptr(out), _ptr(lse), B, Hq,
+        Hkv, d, int(w0), int(w_pretrained), float(rope_theta), float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, lse
 

@@ -63,6 +63,14 @@ SIGNATURES = {
         _c.c_int, _c.c_int, _c.c_double, _c.c_float,       # w0, w_pretrained, theta, scale
         _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
     ]),
+    "jl_bifocal_decode_varlen": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k_cache, v_cache
+        _c.c_void_p, _c.c_int, _c.c_int,                   # seqlens (device), max_len, Lcap
+        _c.c_void_p, _c.c_void_p,                          # o, lse
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int,            # B, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_double, _c.c_float,       # w0, w_pretrained, theta, scale
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_bifocal_decode_noalloc": (_c.c_int, [
         _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k_cache, v_cache
         _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p,      # L, Lcap, o, lse

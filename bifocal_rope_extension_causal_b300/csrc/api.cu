@@ -274,38 +274,73 @@ size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap) {
   return align_up(decode_workspace_bytes(B, Hq, d, Lcap));
 }
 
-int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
-                      void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
-                      double rope_theta, float softmax_scale, void* workspace,
-                      size_t workspace_bytes, void* cuda_stream) {
-  t_err[0] = '\0';
-  if (!q || !k_cache || !v_cache || !o) return fail(JL_ERR_INVALID, "decode: null q/cache/o pointer");
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1)
-    return fail(JL_ERR_INVALID, "decode: need B, Hq, Hkv, Lcap >= 1");
-  if (L < 1 || L > Lcap) return fail(JL_ERR_INVALID, "decode: need 1 <= L <= Lcap (got L=%d, Lcap=%d)", L, Lcap);
-  if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "decode: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
-  if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "decode: need w0 >= 0, w_pretrained >= 1");
-  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "decode: rope_theta must be > 0");
-  if (d != 128) return fail(JL_ERR_UNSUPPORTED, "decode: head dim %d (supported: 128)", d);
+}  // extern "C"
+
+namespace {
+
+// Validation shared by the decode entry points; L is the (largest) length.
+int check_decode(const char* who, const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
+                 const void* o, int B, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta) {
+  if (!q || !k_cache || !v_cache || !o) return fail(JL_ERR_INVALID, "%s: null q/cache/o pointer", who);
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1) return fail(JL_ERR_INVALID, "%s: need B, Hq, Hkv, Lcap >= 1", who);
+  if (L < 1 || L > Lcap) return fail(JL_ERR_INVALID, "%s: need 1 <= L <= Lcap (got L=%d, Lcap=%d)", who, L, Lcap);
+  if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "%s: Hq %% Hkv != 0 (%d, %d)", who, Hq, Hkv);
+  if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "%s: need w0 >= 0, w_pretrained >= 1", who);
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "%s: rope_theta must be > 0", who);
+  if (d != 128) return fail(JL_ERR_UNSUPPORTED, "%s: head dim %d (supported: 128)", who, d);
   const int GQ = Hq / Hkv;
   if (Hkv > 8 || (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8))
-    return fail(JL_ERR_UNSUPPORTED, "decode: need Hkv <= 8 and Hq/Hkv in {1,2,4,8} (got %d, %d)", Hkv, GQ);
+    return fail(JL_ERR_UNSUPPORTED, "%s: need Hkv <= 8 and Hq/Hkv in {1,2,4,8} (got %d, %d)", who, Hkv, GQ);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
-    return fail(JL_ERR_INVALID, "decode: every pointer must be 16-byte aligned");
-  const size_t need = jl_bifocal_decode_workspace_size(B, Hq, d, Lcap);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
-    return fail(JL_ERR_WORKSPACE, "decode: workspace needs %zu bytes, 256-byte aligned (got %zu)", need,
-                workspace_bytes);
+    return fail(JL_ERR_INVALID, "%s: every pointer must be 16-byte aligned", who);
+  return JL_OK;
+}
+
+int run_decode(const char* who, const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+               int L, int Lcap, void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+               double rope_theta, float softmax_scale, void* workspace, size_t workspace_bytes,
+               void* cuda_stream) {
+  int rc = check_decode(who, q, k_cache, v_cache, L, Lcap, o, B, Hq, Hkv, d, w0, w_pretrained, rope_theta);
+  if (rc != JL_OK) return rc;
+  rc = check_workspace(who, workspace, workspace_bytes, jl_bifocal_decode_workspace_size(B, Hq, d, Lcap));
+  if (rc != JL_OK) return rc;
   DecodeArgs a;
   a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.o = o; a.lse = lse;
   a.part = static_cast<float*>(workspace);
+  a.seqlens = seqlens;
   a.B = B; a.L = L; a.Lcap = Lcap; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0;
   a.G = static_cast<int>(jl::group_size(L, w_pretrained));
+  a.wp = w_pretrained;
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
   a.freqs = make_rope_freqs(d, rope_theta);
   const cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
   return JL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
+                      void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                      double rope_theta, float softmax_scale, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  return run_decode("decode", q, k_cache, v_cache, nullptr, L, Lcap, o, lse, B, Hq, Hkv, d, w0, w_pretrained,
+                    rope_theta, softmax_scale, workspace, workspace_bytes, cuda_stream);
+}
+
+int jl_bifocal_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                             const int* seqlens, int max_len, int Lcap, void* o, float* lse, int B,
+                             int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!seqlens || (reinterpret_cast<uintptr_t>(seqlens) % alignof(int)))
+    return fail(JL_ERR_INVALID, "decode_varlen: seqlens must be a non-null, int-aligned device pointer");
+  return run_decode("decode_varlen", q, k_cache, v_cache, seqlens, max_len, Lcap, o, lse, B, Hq, Hkv, d, w0,
+                    w_pretrained, rope_theta, softmax_scale, workspace, workspace_bytes, cuda_stream);
 }
 
 int jl_device_status(void* cuda_stream) {
@@ -320,7 +355,9 @@ int jl_device_status(void* cuda_stream) {
     const int zero = 0;
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "status: clear");
-    return fail(JL_ERR_TIMEOUT, "a bounded device wait ran out (code %d)", h);
+    const char* what = h == 30 ? "a per-sequence length was outside [1, Lcap] and was clamped"
+                               : "a bounded device wait ran out; the kernel skipped its remaining work";
+    return fail(JL_ERR_TIMEOUT, "device status %d: %s", h, what);
   }
   return JL_OK;
 }

@@ -66,7 +66,9 @@ struct DecodeKParams {
   const __nv_bfloat16* vc;
   float* part_o;   // [nsplit, B, Hq, 128]
   float* part_ml;  // [nsplit, B, Hq, 2]
-  int B, L, Lcap, Hq, Hkv, w0, G, keys_per_split;
+  int* status;     // device status word
+  const int* seqlens;  // per-sequence lengths [B] (device) or nullptr: every sequence has length L
+  int B, L, Lcap, Hq, Hkv, w0, G, wp, keys_per_split;
   float scale_log2;
   RopeFreqs freqs;
 };
@@ -145,10 +147,21 @@ decode_partial_kernel(DecodeKParams p) {
   const int warp = tid >> 5, lane = tid & 31;
   const int half = lane >> 4, m = lane & 15;
   const int b = blockIdx.y, split = blockIdx.x;
+  // This sequence's length (the new token is at position L - 1) and group
+  // size; per-sequence lengths outside [1, Lcap] are clamped and flagged.
+  int L = p.L, G = p.G;
+  if (p.seqlens != nullptr) {
+    L = p.seqlens[b];
+    if (L < 1 || L > p.Lcap) {
+      if (threadIdx.x == 0 && split == 0) atomicCAS(p.status, 0, 30);
+      L = min(max(L, 1), p.Lcap);
+    }
+    G = static_cast<int>(group_size(L, p.wp));
+  }
   const int js = split * p.keys_per_split;
-  const int je = min(p.L, js + p.keys_per_split);
-  const int qpos = p.L - 1;
-  const bool bifocal = p.G > 1;
+  const int je = max(js, min(L, js + p.keys_per_split));  // empty slice past the sequence end
+  const int qpos = L - 1;
+  const bool bifocal = G > 1;
   const int first_local = qpos - p.w0;  // keys j >= first_local are local
 
   // kWarpsPerHead warps per KV head: warp `par` of a head takes the global
@@ -190,7 +203,7 @@ decode_partial_kernel(DecodeKParams p) {
   // Query rotations R_{L-1} and R_{f(L-1)}, and the small rotation tables.
   for (int i = tid; i < 64; i += nthr) {
     s_qcs[0][i] = rope_cos_sin(qpos, p.freqs.w[i]);
-    s_qcs[1][i] = rope_cos_sin(alias(qpos, p.G), p.freqs.w[i]);
+    s_qcs[1][i] = rope_cos_sin(alias(qpos, G), p.freqs.w[i]);
   }
   const bool any_remote = bifocal && js < first_local;
   if (any_remote) {
@@ -208,7 +221,7 @@ decode_partial_kernel(DecodeKParams p) {
       const float2 rr = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
       (r < 8 ? s_lo : s_hi)[(r < 8 ? r : r - 8) * 64 + i] = make_float2(rr.x, -rr.y);  // R_{-n}
     }
-    for (int i = tid; i < 64; i += nthr) s_base[i] = rope_cos_sin(alias_offset(js, p.G), p.freqs.w[i]);
+    for (int i = tid; i < 64; i += nthr) s_base[i] = rope_cos_sin(alias_offset(js, G), p.freqs.w[i]);
   }
   __syncthreads();
   const __nv_bfloat16* qin = p.q + static_cast<long long>(b) * p.Hq * kD;
@@ -246,15 +259,15 @@ decode_partial_kernel(DecodeKParams p) {
       __syncthreads();  // previous table no longer read; q (first pass) written
       if (bifocal && j0 < first_local) {
         if (blk > 0) {
-          const int n = alias_offset(j0 - kBlockKeys, p.G) - alias_offset(j0, p.G);  // 0..64
+          const int n = alias_offset(j0 - kBlockKeys, G) - alias_offset(j0, G);  // 0..64
           for (int i = tid; i < 64; i += nthr)
             s_base[i] = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
           __syncthreads();
         }
-        const int fj0 = alias(j0, p.G);
+        const int fj0 = alias(j0, G);
         for (int idx = tid; idx < kBlockKeys * 64; idx += nthr) {
           const int t = idx / 64, i = idx % 64;
-          const int n = t - (alias(j0 + t, p.G) - fj0);  // 0..63
+          const int n = t - (alias(j0 + t, G) - fj0);  // 0..63
           const float2 cs = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
           s_c[idx] = cs.x;
           s_s[idx] = cs.y;
@@ -603,7 +616,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.part_o = a.part;
   p.part_ml = a.part + static_cast<size_t>(kMaxSplits) * a.B * a.Hq * kD;
   p.B = a.B; p.L = a.L; p.Lcap = a.Lcap; p.Hq = a.Hq; p.Hkv = a.Hkv;
-  p.w0 = a.w0; p.G = a.G; p.keys_per_split = bps * kBlockKeys;
+  p.w0 = a.w0; p.G = a.G; p.wp = a.wp; p.keys_per_split = bps * kBlockKeys;
+  p.seqlens = a.seqlens;
+  p.status = device_status_ptr();
+  if (p.status == nullptr) return cudaErrorInvalidSymbol;
   p.scale_log2 = a.scale_log2;
   p.freqs = a.freqs;
 

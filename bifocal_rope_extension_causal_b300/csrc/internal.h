@@ -69,7 +69,8 @@ struct DecodeArgs {
   void* o;              // bf16 [B, Hq, d]
   float* lse;           // fp32 [B, Hq] or nullptr
   float* part;          // workspace: partial outputs and statistics
-  int B, L, Lcap, Hq, Hkv, d, w0, G;
+  const int* seqlens;   // per-sequence lengths [B] on the device, or nullptr
+  int B, L, Lcap, Hq, Hkv, d, w0, G, wp;  // L: the length, or the largest one with seqlens
   float scale_log2;
   RopeFreqs freqs;
 };

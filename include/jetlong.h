@@ -189,6 +189,25 @@ int jl_bifocal_decode(const void* q, const void* k_cache, const void* v_cache,
                       void* cuda_stream);
 
 /*
+ * Batched decode with one length per sequence: sequence b holds
+ * seqlens[b] valid cache positions (its new token at position seqlens[b]-1)
+ * and uses its own G = jl_group_size(seqlens[b], w_pretrained).  Same
+ * arguments and kernels as jl_bifocal_decode otherwise.
+ *
+ *  seqlens  int32 [B] on the DEVICE; each value in [1, max_len] (values
+ *           outside [1, Lcap] are clamped and reported by jl_device_status)
+ *  max_len  largest value of seqlens (<= Lcap); sizes the key split
+ *  workspace >= jl_bifocal_decode_workspace_size(B, Hq, d, Lcap) bytes
+ */
+int jl_bifocal_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                             const int* seqlens, int max_len, int Lcap, void* o, float* lse,
+                             int B, int Hq, int Hkv, int d,
+                             int w0, int w_pretrained, double rope_theta,
+                             float softmax_scale,
+                             void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+
+/*
  * jl_bifocal_decode for callers that cannot allocate device memory.  There is
  * no counterpart on the paper's pages: this is a deployment variant.
  *
@@ -219,8 +238,9 @@ size_t jl_bifocal_decode_noalloc_scratch_bytes(void);
 /*
  * Synchronises `cuda_stream`, then reads and clears the library's device
  * status word, which a kernel sets when one of its bounded waits on a
- * barrier runs out (it then skips its remaining work instead of hanging).
- * Returns JL_OK, JL_ERR_TIMEOUT (message in jl_last_error) or JL_ERR_CUDA.
+ * barrier runs out (it then skips its remaining work instead of hanging) or
+ * when jl_bifocal_decode_varlen had to clamp a length.  Returns JL_OK,
+ * JL_ERR_TIMEOUT (the code and its meaning in jl_last_error) or JL_ERR_CUDA.
  */
 int jl_device_status(void* cuda_stream);
 

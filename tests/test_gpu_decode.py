@@ -81,3 +81,36 @@ def test_decode_matches_prefill_rows(jl):
         assert np.abs(to_np(o_dec) - to_np(o_pre[:, Lp - 1])).max() <= 3e-2, Lp
         assert np.abs(to_np(lse_dec) - to_np(lse_pre[:, :, Lp - 1])).max() <= 2e-3, Lp
     jl.device_status()
+
+
+@pytest.mark.parametrize("lengths,Hq,Hkv,wp,w0", [
+    ((1, 300, 4097, 9000), 32, 8, 2048, 512),     # G = 1, 1, 3, 5 in one batch
+    ((65, 64, 63, 2), 8, 2, 16, 5),                # around one 64-key block
+    ((5000, 17), 4, 4, 6000, 100),                 # G = 1 everywhere
+])
+def test_decode_varlen(jl, lengths, Hq, Hkv, wp, w0):
+    """Batched decode with per-sequence lengths: each sequence matches the
+    oracle decode at its own length (its own G and query position)."""
+    import torch
+    B, Lcap = len(lengths), max(lengths) + 100
+    kc, vc, qs = synth.decode_inputs(Lcap, Hq, Hkv, 128, sum(lengths), 1, B=B)
+    kcd, vcd = kc.cuda(), vc.cuda()
+    seq = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    o, lse = jl.decode_varlen(qs[0].cuda(), kcd, vcd, seq, w0, wp, 1e4)
+    jl.device_status()
+    for b, L in enumerate(lengths):
+        o_ref, l_ref = oracle.bifocal_decode(qs[0][b:b + 1].float().numpy(), kc[b:b + 1, :L].float().numpy(),
+                                             vc[b:b + 1, :L].float().numpy(), L, w0, wp, 1e4)
+        assert_close(to_np(o[b:b + 1]), to_np(lse[b:b + 1]), o_ref, l_ref, f"sequence {b}, L={L}")
+
+
+def test_decode_varlen_flags_bad_lengths(jl):
+    """A length outside [1, Lcap] is clamped and reported by device_status."""
+    import torch
+    from bifocal_rope_extension_causal_b300 import JetLongError
+    kc, vc, qs = synth.decode_inputs(200, 8, 2, 128, 3, 1, B=2)
+    seq = torch.tensor([150, 999], dtype=torch.int32, device="cuda")
+    jl.decode_varlen(qs[0].cuda(), kc.cuda(), vc.cuda(), seq, 10, 64, 1e4, max_len=200)
+    with pytest.raises(JetLongError):
+        jl.device_status()
+    jl.device_status()  # cleared
