@@ -318,6 +318,26 @@ def run_ours(args):
         dec["frac_of_measured_hbm"].append(round(gbs / hbm, 4))
         dec["frac_of_8tbs"].append(round(gbs / 8000.0, 4))
 
+    # Decode alone: the same calls back to back, away from the prefill (whose
+    # power draw and dirty L2 lines slow the first decodes of a step).
+    dec["us_alone"], dec["gbs_alone"], dec["frac_alone_of_measured_hbm"] = [], [], []
+    for i, L in enumerate(dw.lengths):
+        for _ in range(3):
+            decode(i, L)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(20):
+            decode(i, L)
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / 20
+        gbs = dec["bytes"][i] / (us * 1e-6) / 1e9
+        dec["us_alone"].append(round(us, 2))
+        dec["gbs_alone"].append(round(gbs, 1))
+        dec["frac_alone_of_measured_hbm"].append(round(gbs / hbm, 4))
+    jl.device_status()
+
     e2e = run_e2e(jl, q, k, v, w, dev, min(args.steps, 3), world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

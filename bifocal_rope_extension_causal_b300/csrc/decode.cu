@@ -8,8 +8,8 @@
 //
 // Work split.  The key range [0, L) is cut into `nsplit` contiguous slices
 // (whole 64-key blocks), one CTA each, about one per SM; a CTA covers all KV
-// heads of its slice (warp w <-> KV head w), so the per-key rotation tables
-// are built once and shared by all heads.  Each CTA writes an unnormalised
+// heads of its slice (two warps per KV head), so the per-key rotation table
+// is built once and shared by all heads.  Each CTA writes an unnormalised
 // partial (running max m, sum l, sum p v) per query head; a second kernel,
 // launched as a programmatic dependent of the first, merges the slices with
 // log-sum-exp weights.
@@ -17,23 +17,33 @@
 // Memory path.  kWarpsPerHead warps per KV head take alternate 8-key steps;
 // each streams its head's K and V rows (256 B each per key) through its own
 // kStages-deep shared-memory ring with 16-byte cp.async copies (16 lanes per
-// row: fully coalesced; keys past the slice end are zero-filled).
+// row: fully coalesced; keys past the slice end are zero-filled).  The
+// 16-byte chunks of a row are XOR-swizzled by the key index so that the
+// 8x8 ldmatrix tiles read below are free of bank conflicts.
+//
+// Arithmetic.  The per-key work runs on the tensor cores (warp-level
+// mma.sync, bf16 operands, fp32 accumulation), which leaves the CUDA cores
+// only the key rotation and the softmax; issue, not HBM, bounds the plain
+// CUDA-core form of this loop.  Precision is kept at fp32 level by splitting
+// every operand that is not already bf16 into bf16 hi + lo parts:
+//   scores (m16n8k16)  A = the step's 8 keys, corrected by R_{Delta_k} in
+//                      fp32 and split (rows 0..7 hi, rows 8..15 lo);
+//                      B = the pre-scaled rotated query heads of the KV
+//                      head as (hi, lo) column pairs.  The four products of
+//                      a (key, head) land in one lane's accumulator.
+//   O += P V (m16n8k8) computed as O^T += V^T P^T: A = V^T from transposed
+//                      ldmatrix tiles, B = P split as hi + lo (with at most
+//                      four query heads per KV head the lo parts fill the
+//                      idle columns 4..7).
+// The softmax runs in the score fragment (one lane per (key, head)) with
+// lazily raised maxima.
 //
 // Rotation accuracy.  Delta(j) reaches ~1e5, so its angle is reduced in
 // double precision once per CTA (first block); later blocks step the base
 // by R_{-n} with 0 <= n <= 64 from a per-CTA table, and within a block
 // key j0 + t uses base(j0) * R_{-n(t)}.  The R_{-n} table is built from
-// accurately reduced powers of two, R_{-2^b}, with the frequency split in
-// two floats so that 2^b * omega_hi is exact.
-//
-// Lane layout.  A warp takes 8 keys per step: half-warp `half` (lane >> 4)
-// holds keys of parity `half`, lane m = lane & 15 holds head-dim elements
-// 4m..4m+3 and 64+4m..64+4m+3 (the rotate-half partners).  Rotation, dot
-// products and the P V update use packed two-wide fp32 FMAs.  The 16-lane
-// partial dot products of the step's GQ x 4 (head, key) scores are summed
-// with one transpose-reduction that leaves each sum in one lane, and the
-// softmax runs once per (head, key) through a small per-warp exchange
-// buffer in shared memory.
+// R_{-b} and R_{-8a} with the frequency split in two floats so that
+// n * omega_hi is exact.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -49,16 +59,15 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBlockKeys = 64;  // keys per rotation-table block
 constexpr int kStep = 8;        // keys per warp step
-constexpr int kSlots = kStep / 2;
 constexpr int kStages = 2;      // per-warp ring depth
-constexpr int kWarpsPerHead = 2;  // warps sharing a KV head (alternate steps)
+// Warps sharing a KV head (alternate steps): two while the query fragments
+// of a head group fit the 128-register budget of a 512-thread CTA, one for
+// eight query heads per KV head.
+__host__ __device__ constexpr int warps_per_head(int gq) { return gq <= 4 ? 2 : 1; }
 constexpr int kMaxSplits = 512;
 constexpr int kStageBytes = kStep * 2 * kD * 2;  // K and V rows of one step
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
-
-// Per-warp exchange buffer (z[GQ][8], p[8][GQ], alpha[GQ]) in floats, padded
-// to 16 bytes so that the cp.async ring after it stays 16-byte aligned.
-__host__ __device__ constexpr int exchange_floats(int gq) { return (17 * gq + 3) / 4 * 4; }
+constexpr int kTabStride = 36;  // float4 per key row of the rotation table (32 + 4 padding)
 
 struct DecodeKParams {
   const __nv_bfloat16* q;
@@ -83,60 +92,71 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// Four bf16 (two 32-bit words) to two float pairs.
-__device__ __forceinline__ void unpack4(uint2 u, float2& a, float2& b) {
-  a = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
-  b = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
-
 __device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
 
-// Sum the V values of every lane over the 16 lanes of a half-warp.  On
-// return lane m holds kOut = max(1, V / 16) full sums v[0..kOut), which are
-// the original indices (m / kDup) * kOut + k, kDup = max(1, 16 / V).
-template <int V>
-__device__ __forceinline__ void transpose_reduce(float (&v)[V], int m) {
-  int n = V;
-#pragma unroll
-  for (int b = 3; b >= 0; --b) {
-    const int sh = 1 << b;
-    if (n > 1) {
-      const bool up = (m >> b) & 1;
-      const int hf = n / 2;
-#pragma unroll
-      for (int k = 0; k < V / 2; ++k) {
-        if (k < hf) {
-          const float send = up ? v[k] : v[k + hf];
-          const float keep = up ? v[k + hf] : v[k];
-          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
-        }
-      }
-      n = hf;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], sh);
-    }
-  }
+// ---- warp-level tensor-core primitives (bf16 in, fp32 accumulate) ----
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+// Two floats to bf16x2 (x in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): the pair carries
+// about 16 significant bits of each element.
+__device__ __forceinline__ void split_bf16(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v.x, v.y);
+  const float2 r = __ffma2_rn(unpack_bf16(hi), make_float2(-1.f, -1.f), v);
+  lo = pack_bf16(r.x, r.y);
 }
 
 template <int GQ>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(warps_per_head(GQ) * 256, 1)
 decode_partial_kernel(DecodeKParams p) {
-  constexpr int kV = GQ * kSlots;                 // scores per half-warp per step
-  constexpr int kOut = kV >= 16 ? kV / 16 : 1;    // sums held per lane after the reduction
-  constexpr int kDup = kV >= 16 ? 1 : 16 / kV;    // lanes holding the same sum
-  constexpr int kOwn = (GQ * 8 + 31) / 32;        // (head, key) pairs per lane in the softmax
+  constexpr int kWarpsPerHead = warps_per_head(GQ);
+  constexpr int kNT = (GQ + 3) / 4;                // score n-tiles: 4 heads x {hi, lo} each
   constexpr int kBlockSteps = kBlockKeys / kStep;  // global steps per table block (8)
+  // P V columns: with GQ <= 4, column n holds head n & 3, its P hi part for
+  // n < 4 and its lo part for n >= 4; with GQ = 8 column n is head n.
+  constexpr bool kLoCols = GQ <= 4;
+  auto hcol = [](int n) { return kLoCols ? (n & 3) : n; };
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int nwarps = blockDim.x >> 5;
-  float* s_qa = reinterpret_cast<float*>(smem_raw);                 // [Hq][128], pre-scaled
-  float* s_qr = s_qa + p.Hq * kD;                                   // [Hq][128]
-  float* s_c = s_qr + p.Hq * kD;                                    // [64 keys][64] cos
-  float* s_s = s_c + kBlockKeys * 64;                               // [64 keys][64] sin
-  float2* s_lo = reinterpret_cast<float2*>(s_s + kBlockKeys * 64);  // [8][64]: R_{-b}
-  float2* s_hi = s_lo + 8 * 64;                                     // [9][64]: R_{-8a}
-  float2* s_base = s_hi + 9 * 64;                                   // [64]
-  float* s_x = reinterpret_cast<float*>(s_base + 64);               // per-warp exchange buffers
-  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_x + nwarps * exchange_floats(GQ));
+  // Region A: the rotated queries during set-up, then the rotation table of
+  // the current 64-key block: [key][kTabStride] float4 {cos_i, cos_i+1,
+  // sin_i, sin_i+1} for the frequency pair (i, i+1), i = 2 * index.
+  float* s_qa = reinterpret_cast<float*>(smem_raw);  // [Hq][128], pre-scaled
+  float* s_qr = s_qa + p.Hq * kD;                    // [Hq][128]
+  const float4* s_tab = reinterpret_cast<const float4*>(smem_raw);
+  float4* s_tab_w = reinterpret_cast<float4*>(smem_raw);
+  const int region_a = max(2 * p.Hq * kD * 4, kBlockKeys * kTabStride * 16);
+  float2* s_lo = reinterpret_cast<float2*>(smem_raw + region_a);  // [8][64]: R_{-b}
+  float2* s_hi = s_lo + 8 * 64;                                   // [9][64]: R_{-8a}
+  float2* s_base = s_hi + 9 * 64;                                 // [64]
+  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_base + 64);
   __shared__ float2 s_qcs[2][64];
 
   // Let the merge kernel (a programmatic dependent) launch early; it waits
@@ -145,7 +165,7 @@ decode_partial_kernel(DecodeKParams p) {
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int half = lane >> 4, m = lane & 15;
+  const int g = lane >> 2, t4 = lane & 3;  // fragment row group / column pair
   const int b = blockIdx.y, split = blockIdx.x;
   // This sequence's length (the new token is at position L - 1) and group
   // size; per-sequence lengths outside [1, Lcap] are clamped and flagged.
@@ -172,27 +192,42 @@ decode_partial_kernel(DecodeKParams p) {
   const __nv_bfloat16* vbase = p.vc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
   unsigned char* my_ring = s_ring + warp * kStages * kStageBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(my_ring));
-  float* xz = s_x + warp * exchange_floats(GQ);  // z[GQ][8]
-  float* xp = xz + 8 * GQ;                       // p[8][GQ]
-  float* xa = xp + 8 * GQ;                       // alpha[GQ]
   const int nsteps = (je - js + kStep - 1) / kStep;
   const int nlocal = (nsteps + kWarpsPerHead - 1) / kWarpsPerHead;  // local steps (warp 0 of a head)
 
   // Stage layout: K rows of the step's 8 keys (256 B each), then V rows.
+  // 16-byte chunk c of key row r sits at chunk c ^ (r & 7) of its row, so
+  // that the eight rows of an 8x8 ldmatrix tile fall in eight bank groups.
+  // Lane roles of the copies: chunk c = lane & 15 of key 2 i + (lane >> 4).
+  const long long lane_src = static_cast<long long>(lane >> 4) * row_stride + (lane & 15) * 8;
+  // Destination of copy i (key 2 i + (lane >> 4), swizzled chunk), relative to the stage.
+  uint32_t lane_dst[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int key = 2 * i + (lane >> 4);
+    lane_dst[i] = static_cast<uint32_t>((key * 16 + ((lane & 15) ^ key)) * 16);
+  }
   auto issue_step = [&](int u) {
     const int it = kWarpsPerHead * u + par;
     if (it < nsteps) {
       const int jstep = js + it * kStep;
       const uint32_t st = ring + static_cast<uint32_t>((u % kStages) * kStageBytes);
+      if (jstep + kStep <= je) {  // full step: no bounds checks
+        const __nv_bfloat16* kp = kbase + lane_src + static_cast<long long>(jstep) * row_stride;
+        const __nv_bfloat16* vp = vbase + lane_src + static_cast<long long>(jstep) * row_stride;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = i * 32 + lane;  // 256 chunks of 16 B
-        const int tensor = idx >> 7, key = (idx >> 4) & 7, c = idx & 15;
-        const int j = jstep + key;
-        const bool ok = j < je;
-        const __nv_bfloat16* src =
-            (tensor ? vbase : kbase) + (ok ? static_cast<long long>(j) * row_stride : 0) + c * 8;
-        cp_async16(st + static_cast<uint32_t>(idx * 16), src, ok ? 16 : 0);
+        for (int i = 0; i < 4; ++i) {
+          cp_async16(st + lane_dst[i], kp + 2 * i * row_stride, 16);
+          cp_async16(st + 2048 + lane_dst[i], vp + 2 * i * row_stride, 16);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool ok = jstep + 2 * i + (lane >> 4) < je;
+          const long long off = ok ? lane_src + static_cast<long long>(jstep + 2 * i) * row_stride : 0;
+          cp_async16(st + lane_dst[i], kbase + off, ok ? 16 : 0);
+          cp_async16(st + 2048 + lane_dst[i], vbase + off, ok ? 16 : 0);
+        }
       }
     }
     cp_async_commit();
@@ -236,19 +271,44 @@ decode_partial_kernel(DecodeKParams p) {
     s_qr[h * kD + i] = rr.x * p.scale_log2;
     s_qr[h * kD + 64 + i] = rr.y * p.scale_log2;
   }
-  // (The first table build below starts with a barrier.)
+  __syncthreads();
+  // Query operands of the score MMA (B, 16 dims x 8 columns per chunk):
+  // column n of n-tile nt is head 4 nt + n / 2, hi part (n even) or lo part
+  // (n odd) of the pre-scaled rotated query; variant 0 absolute, 1 aliased.
+  uint32_t qf[2][kNT][8][2];
+#pragma unroll
+  for (int v = 0; v < 2; ++v)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int hl = 4 * nt + (g >> 1);
+      const float* qrow = (v ? s_qr : s_qa) + (hk * GQ + (hl < GQ ? hl : 0)) * kD;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t hi, lo;
+          split_bf16(*reinterpret_cast<const float2*>(qrow + 16 * c + 8 * e + 2 * t4), hi, lo);
+          qf[v][nt][c][e] = hl < GQ ? ((g & 1) ? lo : hi) : 0u;
+        }
+    }
+  // (The first table build below starts with a barrier, after which the
+  // table may overwrite the rotated queries.)
 
-  float2 o[GQ][4];
+  // O^T accumulators: m-tile mt holds dims 16 mt + g (+8) of heads 2 t4, 2 t4 + 1.
+  float o[8][4];
 #pragma unroll
-  for (int h = 0; h < GQ; ++h)
+  for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
-  float m_run[kOwn], l_run[kOwn];
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+  // Softmax state of head 4 nt + t4 (the same in the 8 lanes of a column).
+  float m_run[kNT], l_run[kNT];
 #pragma unroll
-  for (int k = 0; k < kOwn; ++k) {
-    m_run[k] = -INFINITY;
-    l_run[k] = 0.f;
+  for (int nt = 0; nt < kNT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.f;
   }
+  // ldmatrix lane roles: lanes 8 mi .. 8 mi + 7 address rows 0..7 of tile mi.
+  const int lm = lane >> 3, lr = lane & 7;
 
   constexpr int kBlockLocal = kBlockSteps / kWarpsPerHead;  // local steps per table block
   for (int u = 0; u < nlocal; ++u) {
@@ -256,7 +316,7 @@ decode_partial_kernel(DecodeKParams p) {
     const int blk = u / kBlockLocal;
     const int j0 = js + blk * kBlockKeys;  // table block base
     if ((u % kBlockLocal) == 0) {
-      __syncthreads();  // previous table no longer read; q (first pass) written
+      __syncthreads();  // previous table (or the rotated queries) no longer read
       if (bifocal && j0 < first_local) {
         if (blk > 0) {
           const int n = alias_offset(j0 - kBlockKeys, G) - alias_offset(j0, G);  // 0..64
@@ -265,12 +325,14 @@ decode_partial_kernel(DecodeKParams p) {
           __syncthreads();
         }
         const int fj0 = alias(j0, G);
-        for (int idx = tid; idx < kBlockKeys * 64; idx += nthr) {
-          const int t = idx / 64, i = idx % 64;
+        for (int idx = tid; idx < kBlockKeys * 32; idx += nthr) {
+          const int t = idx >> 5, pp = idx & 31, i0 = 2 * pp;
           const int n = t - (alias(j0 + t, G) - fj0);  // 0..63
-          const float2 cs = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
-          s_c[idx] = cs.x;
-          s_s[idx] = cs.y;
+          const float2 c0 =
+              compose(compose(s_base[i0], s_hi[(n >> 3) * 64 + i0]), s_lo[(n & 7) * 64 + i0]);
+          const float2 c1 = compose(compose(s_base[i0 + 1], s_hi[(n >> 3) * 64 + i0 + 1]),
+                                    s_lo[(n & 7) * 64 + i0 + 1]);
+          s_tab_w[t * kTabStride + pp] = make_float4(c0.x, c1.x, c0.y, c1.y);
         }
       }
       __syncthreads();
@@ -281,228 +343,244 @@ decode_partial_kernel(DecodeKParams p) {
     if (it >= nsteps) continue;
 
     const int jstep = js + it * kStep;
-    const unsigned char* st = my_ring + (u % kStages) * kStageBytes;
+    const uint32_t st = ring + static_cast<uint32_t>((u % kStages) * kStageBytes);
     const bool all_local = !bifocal || jstep >= first_local;
     const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
 
-    // Full scores of this step's keys; lane m ends with sums (m/kDup)*kOut+k
-    // of the index h * 4 + s (key 2s + half).
-    auto scores = [&](const float* qs, bool rot, float (&zout)[kOut]) {
-      float sc[kV];
+    // Scores z[nt] of (key jstep + g, head 4 nt + t4) in log2 units.
+    float z[kNT];
 #pragma unroll
-      for (int s = 0; s < kSlots; ++s) {
-        const int key = 2 * s + half;
-        float2 x01, x23, y01, y23;
-        unpack4(*reinterpret_cast<const uint2*>(st + key * 256 + 8 * m), x01, x23);
-        unpack4(*reinterpret_cast<const uint2*>(st + key * 256 + 128 + 8 * m), y01, y23);
-        if (rot) {
-          const int t = (jstep - j0) + key;
-          const float4 c = *reinterpret_cast<const float4*>(s_c + t * 64 + 4 * m);
-          const float4 sn = *reinterpret_cast<const float4*>(s_s + t * 64 + 4 * m);
-          const float2 c01 = make_float2(c.x, c.y), c23 = make_float2(c.z, c.w);
-          const float2 s01 = make_float2(sn.x, sn.y), s23 = make_float2(sn.z, sn.w);
-          // (x, y) -> (x c - y s, y c + x s)
-          const float2 nx01 = __ffma2_rn(y01, neg2(s01), __fmul2_rn(x01, c01));
-          const float2 nx23 = __ffma2_rn(y23, neg2(s23), __fmul2_rn(x23, c23));
-          y01 = __ffma2_rn(x01, s01, __fmul2_rn(y01, c01));
-          y23 = __ffma2_rn(x23, s23, __fmul2_rn(y23, c23));
-          x01 = nx01;
-          x23 = nx23;
-        }
+    for (int nt = 0; nt < kNT; ++nt) z[nt] = 0.f;
+    if (!all_local) {
+      // Aliased scores.  A = the step's 8 keys corrected by R_{f(j) - j},
+      // rows 0..7 their bf16 hi parts, rows 8..15 the lo parts; chunk c
+      // (dims 16 c ..) and chunk c + 4 (the rotate-half partners) together.
+      float acc0[kNT][4], acc1[kNT][4];
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-          const float* qh = qs + (hk * GQ + h) * kD;
-          const float4 a = *reinterpret_cast<const float4*>(qh + 4 * m);
-          const float4 c = *reinterpret_cast<const float4*>(qh + 64 + 4 * m);
-          float2 acc = __fmul2_rn(make_float2(a.x, a.y), x01);
-          acc = __ffma2_rn(make_float2(a.z, a.w), x23, acc);
-          acc = __ffma2_rn(make_float2(c.x, c.y), y01, acc);
-          acc = __ffma2_rn(make_float2(c.z, c.w), y23, acc);
-          sc[h * kSlots + s] = acc.x + acc.y;
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc0[nt][e] = acc1[nt][e] = 0.f;
+      const float4* tab = s_tab + (jstep - j0 + g) * kTabStride + t4;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r0, r1, r2, r3;
+        const int ch = 2 * c + (lm & 1) + 8 * (lm >> 1);
+        ldsm_x4(st + static_cast<uint32_t>(lr * 256 + ((ch ^ lr) << 4)), r0, r1, r2, r3);
+        const float4 cs0 = tab[8 * c], cs1 = tab[8 * c + 4];
+        const float2 x0 = unpack_bf16(r0), x1 = unpack_bf16(r1), y0 = unpack_bf16(r2), y1 = unpack_bf16(r3);
+        const float2 c0 = make_float2(cs0.x, cs0.y), s0 = make_float2(cs0.z, cs0.w);
+        const float2 c1 = make_float2(cs1.x, cs1.y), s1 = make_float2(cs1.z, cs1.w);
+        // (x, y) -> (x c - y s, y c + x s)
+        const float2 nx0 = __ffma2_rn(y0, neg2(s0), __fmul2_rn(x0, c0));
+        const float2 ny0 = __ffma2_rn(x0, s0, __fmul2_rn(y0, c0));
+        const float2 nx1 = __ffma2_rn(y1, neg2(s1), __fmul2_rn(x1, c1));
+        const float2 ny1 = __ffma2_rn(x1, s1, __fmul2_rn(y1, c1));
+        uint32_t x0h, x0l, x1h, x1l, y0h, y0l, y1h, y1l;
+        split_bf16(nx0, x0h, x0l);
+        split_bf16(nx1, x1h, x1l);
+        split_bf16(ny0, y0h, y0l);
+        split_bf16(ny1, y1h, y1l);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          mma16816(acc0[nt], x0h, x0l, x1h, x1l, qf[1][nt][c][0], qf[1][nt][c][1]);
+          mma16816(acc1[nt], y0h, y0l, y1h, y1l, qf[1][nt][c + 4][0], qf[1][nt][c + 4][1]);
         }
       }
-      transpose_reduce<kV>(sc, m);
 #pragma unroll
-      for (int k = 0; k < kOut; ++k) zout[k] = sc[k];
-    };
+      for (int nt = 0; nt < kNT; ++nt)
+        z[nt] = ((acc0[nt][0] + acc0[nt][1]) + (acc0[nt][2] + acc0[nt][3])) +
+                ((acc1[nt][0] + acc1[nt][1]) + (acc1[nt][2] + acc1[nt][3]));
+    }
+    if (!all_remote) {
+      // Absolute scores: the cached keys as stored (exact in bf16, lo rows 0).
+      float acc0[kNT][4], acc1[kNT][4];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc0[nt][e] = acc1[nt][e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r0, r1, r2, r3;
+        const int ch = 2 * c + (lm & 1) + 8 * (lm >> 1);
+        ldsm_x4(st + static_cast<uint32_t>(lr * 256 + ((ch ^ lr) << 4)), r0, r1, r2, r3);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          mma16816(acc0[nt], r0, 0u, r1, 0u, qf[0][nt][c][0], qf[0][nt][c][1]);
+          mma16816(acc1[nt], r2, 0u, r3, 0u, qf[0][nt][c + 4][0], qf[0][nt][c + 4][1]);
+        }
+      }
+      const bool local = !bifocal || jstep + g >= first_local;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        const float za = (acc0[nt][0] + acc0[nt][1]) + (acc1[nt][0] + acc1[nt][1]);
+        if (all_local || local) z[nt] = za;
+      }
+    }
 
-    float z[kOut];
-    if (all_local) {
-      scores(s_qa, false, z);
-    } else if (all_remote) {
-      scores(s_qr, true, z);
-    } else {
-      float zr[kOut];
-      scores(s_qa, false, z);
-      scores(s_qr, true, zr);
-#pragma unroll
-      for (int k = 0; k < kOut; ++k) {
-        const int i = (m / kDup) * kOut + k;  // = h * 4 + s
-        if (jstep + 2 * (i % kSlots) + half < first_local) z[k] = zr[k];
-      }
-    }
-    // Publish the step's scores: xz[h][key].
-#pragma unroll
-    for (int k = 0; k < kOut; ++k) {
-      const int i = (m / kDup) * kOut + k;
-      xz[(i / kSlots) * 8 + 2 * (i % kSlots) + half] = z[k];
-    }
-    __syncwarp();
-    // Online softmax, one lane per (head, key); a head's 8 keys are 8
-    // consecutive lanes.  The max used for the exponentials is raised only
-    // when it grows by more than kRescaleThreshold.
+    // Online softmax per head (column); the max used for the exponentials
+    // is raised only when it grows by more than kRescaleThreshold.
     bool any_rescale = false;
+    float pr[kNT], al[kNT];
 #pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-      const int idx = k * 32 + lane;
-      const bool own = idx < GQ * 8;
-      const int h = idx >> 3, key = idx & 7;
-      const bool valid = own && (jstep + key < je);
-      const float zz = valid ? xz[idx] : -INFINITY;
+    for (int nt = 0; nt < kNT; ++nt) {
+      const bool valid = jstep + g < je && 4 * nt + t4 < GQ;
+      const float zz = valid ? z[nt] : -INFINITY;
       float bm = zz;
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
       float alpha = 1.f;
-      if (bm > m_run[k] + kRescaleThreshold) {
-        alpha = exp2f(m_run[k] - bm);
-        m_run[k] = bm;
+      if (bm > m_run[nt] + kRescaleThreshold) {
+        alpha = exp2f(m_run[nt] - bm);
+        m_run[nt] = bm;
       }
-      const float mexp = m_run[k] == -INFINITY ? 0.f : m_run[k];
-      const float pr = exp2f(zz - mexp);
-      l_run[k] = l_run[k] * alpha + pr;
-      if (own) {
-        xp[key * GQ + h] = pr;
-        if (key == 0) xa[h] = alpha;
-      }
+      const float mexp = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
+      pr[nt] = exp2f(zz - mexp);
+      l_run[nt] = l_run[nt] * alpha + pr[nt];
+      al[nt] = alpha;
       any_rescale |= alpha != 1.f;
     }
     any_rescale = __any_sync(0xffffffffu, any_rescale);
-    __syncwarp();
     if (any_rescale) {
+      // Column n of O^T belongs to head hcol(n); its alpha sits in lane
+      // hcol & 3 of n-tile hcol >> 2.
+      float ae = 1.f, ao = 1.f;
+      const int he = hcol(2 * t4), ho = hcol(2 * t4 + 1);
 #pragma unroll
-      for (int h = 0; h < GQ; ++h) {
-        const float a = xa[h];
-        const float2 a2 = make_float2(a, a);
+      for (int nt = 0; nt < kNT; ++nt) {
+        const float x = __shfl_sync(0xffffffffu, al[nt], he & 3);
+        const float y = __shfl_sync(0xffffffffu, al[nt], ho & 3);
+        if ((he >> 2) == nt) ae = x;
+        if ((ho >> 2) == nt) ao = y;
+      }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= ae;
+        o[mt][1] *= ao;
+        o[mt][2] *= ae;
+        o[mt][3] *= ao;
       }
     }
-    // O += P V (keys past the slice end have p = 0 and zero-filled rows).
+    // P^T operand (B, 8 keys x 8 columns): keys 2 t4, 2 t4 + 1 of column g,
+    // i.e. of head hcol(g), from lanes 4 key + (head & 3) of n-tile head >> 2.
+    // P is split as hi + lo in bf16: with GQ <= 4 the lo parts fill columns
+    // 4..7, otherwise they go through a second product.
+    uint32_t pb_hi, pb_lo;
+    {
+      const int hh = hcol(g);
+      const int src = 8 * t4 + (hh & 3);
+      float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      const int key = 2 * s + half;
-      float2 v01, v23, w01, w23;
-      unpack4(*reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 8 * m), v01, v23);
-      unpack4(*reinterpret_cast<const uint2*>(st + (kStep + key) * 256 + 128 + 8 * m), w01, w23);
-      float pk[GQ];
-      if constexpr (GQ % 4 == 0) {
-#pragma unroll
-        for (int h = 0; h < GQ; h += 4) {
-          const float4 q4 = *reinterpret_cast<const float4*>(xp + key * GQ + h);
-          pk[h] = q4.x;
-          pk[h + 1] = q4.y;
-          pk[h + 2] = q4.z;
-          pk[h + 3] = q4.w;
+      for (int nt = 0; nt < kNT; ++nt) {
+        const float a = __shfl_sync(0xffffffffu, pr[nt], src);
+        const float c = __shfl_sync(0xffffffffu, pr[nt], src + 4);
+        if ((hh >> 2) == nt) {
+          p0 = a;
+          p1 = c;
         }
-      } else {
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) pk[h] = xp[key * GQ + h];
       }
-#pragma unroll
-      for (int h = 0; h < GQ; ++h) {
-        const float2 p2 = make_float2(pk[h], pk[h]);
-        o[h][0] = __ffma2_rn(p2, v01, o[h][0]);
-        o[h][1] = __ffma2_rn(p2, v23, o[h][1]);
-        o[h][2] = __ffma2_rn(p2, w01, o[h][2]);
-        o[h][3] = __ffma2_rn(p2, w23, o[h][3]);
+      uint32_t hi, lo;
+      split_bf16(make_float2(p0, p1), hi, lo);
+      const bool use = hh < GQ;
+      if constexpr (kLoCols) {
+        pb_hi = use ? (g < 4 ? hi : lo) : 0u;
+        pb_lo = 0u;
+      } else {
+        pb_hi = use ? hi : 0u;
+        pb_lo = use ? lo : 0u;
       }
     }
-    __syncwarp();  // the stage and the exchange buffer are rewritten next step
+    // O^T += V^T P^T: four transposed 8x8 loads of V give the A operands of
+    // two 16-dim m-tiles each (keys past the slice end have p = 0 and
+    // zero-filled rows).
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      uint32_t v0, v1, v2, v3;
+      const int ch = 4 * jj + lm;
+      ldsm_x4_t(st + static_cast<uint32_t>((kStep + lr) * 256 + ((ch ^ lr) << 4)), v0, v1, v2, v3);
+      mma1688(o[2 * jj], v0, v1, pb_hi);
+      mma1688(o[2 * jj + 1], v2, v3, pb_hi);
+      if constexpr (!kLoCols) {
+        mma1688(o[2 * jj], v0, v1, pb_lo);
+        mma1688(o[2 * jj + 1], v2, v3, pb_lo);
+      }
+    }
+    __syncwarp();  // the stage is rewritten next step
   }
   cp_async_wait<0>();
 
-  // Per-head statistics of this warp: m (shared by the head's 8 lanes) and
-  // l summed over them; combine the two key parities of o within the warp.
-  float mh[kOwn], lh[kOwn];
+  // Per-head statistics of this warp: l summed over the 8 key lanes.
+  float lh[kNT];
 #pragma unroll
-  for (int k = 0; k < kOwn; ++k) {
-    float l = l_run[k];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
+  for (int nt = 0; nt < kNT; ++nt) {
+    float l = l_run[nt];
     l += __shfl_xor_sync(0xffffffffu, l, 4);
-    mh[k] = m_run[k];
-    lh[k] = l;
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    lh[nt] = l;
   }
-#pragma unroll
-  for (int h = 0; h < GQ; ++h)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      o[h][e].x += __shfl_xor_sync(0xffffffffu, o[h][e].x, 16);
-      o[h][e].y += __shfl_xor_sync(0xffffffffu, o[h][e].y, 16);
-    }
-  // With two warps per head, the second hands its state to the first
-  // through its (now idle) ring: o [GQ][128] then (m, l) [GQ][2].
+  // Each warp leaves its state in its (now idle) ring: o [GQ][128], then
+  // (m, l) [GQ][2]; the CTA then merges the warps of each KV head.
+  __syncthreads();
   float* hand = reinterpret_cast<float*>(my_ring);
-  if constexpr (kWarpsPerHead == 2) __syncthreads();
-  if (kWarpsPerHead == 2 && par == 1) {
-    if (half == 0) {
+  if constexpr (kLoCols) {
+    // Column n + 4 (lane t4 + 2) holds the lo-part product of column n.
 #pragma unroll
-      for (int h = 0; h < GQ; ++h) {
-        *reinterpret_cast<float4*>(hand + h * kD + 4 * m) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-        *reinterpret_cast<float4*>(hand + h * kD + 64 + 4 * m) =
-            make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
-      }
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d0 = 16 * mt + g;
+    const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+    if (h0 < GQ) {
+      hand[h0 * kD + d0] = o[mt][0];
+      hand[h0 * kD + d0 + 8] = o[mt][2];
     }
-#pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-      const int idx = k * 32 + lane;
-      if (idx < GQ * 8 && (idx & 7) == 0) {
-        hand[GQ * kD + 2 * (idx >> 3)] = mh[k];
-        hand[GQ * kD + 2 * (idx >> 3) + 1] = lh[k];
-      }
+    if (h1 < GQ) {
+      hand[h1 * kD + d0] = o[mt][1];
+      hand[h1 * kD + d0 + 8] = o[mt][3];
     }
   }
-  if constexpr (kWarpsPerHead == 2) __syncthreads();
-  if (par != 0) return;
-  const float* other = reinterpret_cast<const float*>(s_ring + (warp + p.Hkv) * kStages * kStageBytes);
-  const bool paired = kWarpsPerHead == 2;
-  // Merge state of head h: M = max(m0, m1), scales 2^(m0-M), 2^(m1-M).
 #pragma unroll
-  for (int h = 0; h < GQ; ++h) {
-    const float m1 = paired ? other[GQ * kD + 2 * h] : -INFINITY;
-    const float l1 = paired ? other[GQ * kD + 2 * h + 1] : 0.f;
-    // This warp's m and l of head h live in lanes 8h..8h+7 of iteration h / 4.
-    float m0 = 0.f, l0 = 0.f;
-#pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-      const float mk = __shfl_sync(0xffffffffu, mh[k], (h * 8) & 31);
-      const float lk = __shfl_sync(0xffffffffu, lh[k], (h * 8) & 31);
-      if (k == (h * 8) / 32) {
-        m0 = mk;
-        l0 = lk;
-      }
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int h = 4 * nt + t4;
+    if (g == 0 && h < GQ) {
+      hand[GQ * kD + 2 * h] = m_run[nt];
+      hand[GQ * kD + 2 * h + 1] = lh[nt];
     }
-    const float M = fmaxf(m0, m1);
-    const float a0 = M == -INFINITY ? 0.f : exp2f(m0 - M);
-    const float a1 = M == -INFINITY ? 0.f : exp2f(m1 - M);
-    const int hq = hk * GQ + h;
+  }
+  __syncthreads();
+  // Merge: M = max over the head's warps, weights 2^(m_w - M).
+  for (int idx = tid; idx < p.Hq * 32; idx += nthr) {
+    const int hq = idx >> 5, d4 = idx & 31;
+    const int kv = hq / GQ, h = hq % GQ;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerHead; ++w) {
+      const float* src = reinterpret_cast<const float*>(s_ring + (kv + w * p.Hkv) * kStages * kStageBytes);
+      M = fmaxf(M, src[GQ * kD + 2 * h]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerHead; ++w) {
+      const float* src = reinterpret_cast<const float*>(s_ring + (kv + w * p.Hkv) * kStages * kStageBytes);
+      const float mw = src[GQ * kD + 2 * h];
+      const float a = M == -INFINITY ? 0.f : exp2f(mw - M);
+      lsum += a * src[GQ * kD + 2 * h + 1];
+      const float4 v = *reinterpret_cast<const float4*>(src + h * kD + 4 * d4);
+      acc.x += a * v.x;
+      acc.y += a * v.y;
+      acc.z += a * v.z;
+      acc.w += a * v.w;
+    }
     const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
-    if (half == 0) {
-      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 b0 = paired ? *reinterpret_cast<const float4*>(other + h * kD + 4 * m) : zero4;
-      const float4 b1 = paired ? *reinterpret_cast<const float4*>(other + h * kD + 64 + 4 * m) : zero4;
-      float* dst = p.part_o + slot * kD;
-      *reinterpret_cast<float4*>(dst + 4 * m) =
-          make_float4(a0 * o[h][0].x + a1 * b0.x, a0 * o[h][0].y + a1 * b0.y, a0 * o[h][1].x + a1 * b0.z,
-                      a0 * o[h][1].y + a1 * b0.w);
-      *reinterpret_cast<float4*>(dst + 64 + 4 * m) =
-          make_float4(a0 * o[h][2].x + a1 * b1.x, a0 * o[h][2].y + a1 * b1.y, a0 * o[h][3].x + a1 * b1.z,
-                      a0 * o[h][3].y + a1 * b1.w);
-    }
-    if (lane == 0) {
+    *reinterpret_cast<float4*>(p.part_o + slot * kD + 4 * d4) = acc;
+    if (d4 == 0) {
       p.part_ml[slot * 2] = M;
-      p.part_ml[slot * 2 + 1] = a0 * l0 + a1 * l1;
+      p.part_ml[slot * 2 + 1] = lsum;
     }
   }
 }
@@ -623,11 +701,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.freqs = a.freqs;
 
-  const int warps = kWarpsPerHead * a.Hkv;
-  const size_t smem = static_cast<size_t>(2) * a.Hq * kD * sizeof(float) +           // q
-                      static_cast<size_t>(2) * kBlockKeys * 64 * sizeof(float) +     // cos, sin
-                      static_cast<size_t>(8 + 9 + 1) * 64 * sizeof(float2) +         // R_-b, R_-8a, base
-                      static_cast<size_t>(warps) * exchange_floats(GQ) * sizeof(float) +
+  const int warps = warps_per_head(GQ) * a.Hkv;
+  const size_t region_a = std::max(static_cast<size_t>(2) * a.Hq * kD * sizeof(float),    // q
+                                    static_cast<size_t>(kBlockKeys) * kTabStride * 16);     // rotation table
+  const size_t smem = region_a + static_cast<size_t>(8 + 9 + 1) * 64 * sizeof(float2) +   // R_-b, R_-8a, base
                       static_cast<size_t>(warps) * kStages * kStageBytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   const dim3 grid(nsplit, a.B);
