@@ -318,20 +318,33 @@ def run_ours(args):
         dec["frac_of_measured_hbm"].append(round(gbs / hbm, 4))
         dec["frac_of_8tbs"].append(round(gbs / 8000.0, 4))
 
-    # Decode alone: the same calls back to back, away from the prefill (whose
-    # power draw and dirty L2 lines slow the first decodes of a step).
+    # Decode alone, away from the prefill (whose power draw and dirty L2
+    # lines slow the first decodes of a step): 20 calls at one length
+    # captured in a CUDA graph and replayed, so host call overhead is not
+    # timed.
     dec["us_alone"], dec["gbs_alone"], dec["frac_alone_of_measured_hbm"] = [], [], []
+    n_rep = 20
     for i, L in enumerate(dw.lengths):
-        for _ in range(3):
-            decode(i, L)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):  # warm-up on the capture stream
+                jl.decode(qs[i], kc, vc, L, dw.w0, dw.w_pretrained, dw.theta, out=od, lse=lsed,
+                          workspace=dws)
+        side.synchronize()
+        with torch.cuda.graph(graph):
+            for _ in range(n_rep):
+                jl.decode(qs[i], kc, vc, L, dw.w0, dw.w_pretrained, dw.theta, out=od, lse=lsed,
+                          workspace=dws)
+        graph.replay()
         torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(20):
-            decode(i, L)
+        graph.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        us = 1e3 * a.elapsed_time(b) / 20
+        us = 1e3 * a.elapsed_time(b) / n_rep
         gbs = dec["bytes"][i] / (us * 1e-6) / 1e9
         dec["us_alone"].append(round(us, 2))
         dec["gbs_alone"].append(round(gbs, 1))
@@ -429,6 +442,49 @@ def run_profile_prefill(args):
     flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
     print(json.dumps({"profile_prefill_L": L, "G": jl.group_size(L, w.w_pretrained), "ms": ms,
                       "tflops": flops / (ms * 1e-3) / 1e12}))
+    return 0
+
+
+def run_profile_three_pass(args):
+    """A/B of the two forms of the same prefill on the 4x-extension shapes at
+    sequence length L: the routed single pass against the three-pass
+    inclusion-exclusion form (two window passes, one full aliased pass, one
+    merge).  Reports both times, the single pass's algorithmic TFLOP/s for
+    each, and the largest difference between their outputs."""
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    w = PREFILL
+    L = int(args.profile_three_pass)
+    dev = torch.device("cuda", 0)
+    q, k, v = synth.prefill_inputs(L, w.Hq, w.Hkv, w.d, w.index)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws1 = jl.alloc_workspace(jl.prefill_workspace_size(1, L, w.Hq, w.Hkv, w.d, w.w_pretrained), dev)
+    ws3 = jl.alloc_workspace(jl.load().jl_bifocal_prefill_three_pass_workspace_size(
+        1, L, w.Hq, w.Hkv, w.d, w.w_pretrained), dev)
+    runs = {"single": lambda: jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws1),
+            "three_pass": lambda: jl.prefill_three_pass(qd, kd, vd, w.w0, w.w_pretrained, w.theta,
+                                                        workspace=ws3)}
+    flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
+    res, outs = {}, {}
+    for name, run in runs.items():
+        for _ in range(args.warmup):
+            outs[name] = run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        jl.device_status()
+        ms = a.elapsed_time(b) / args.steps
+        res[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+    (o1, l1), (o3, l3) = outs["single"], outs["three_pass"]
+    do = (o1.float() - o3.float()).abs()
+    print(json.dumps({"profile_three_pass_L": L, "G": jl.group_size(L, w.w_pretrained), **res,
+                      "ratio_three_over_single": round(res["three_pass"]["ms"] / res["single"]["ms"], 3),
+                      "o_maxabs_diff": float(do.max()), "o_meanabs_diff": float(do.mean()),
+                      "lse_maxabs_diff": float((l1 - l3).abs().max())}))
     return 0
 
 
@@ -541,6 +597,8 @@ def main():
     ap.add_argument("--profile-chunked", type=int, nargs=2, default=None, metavar=("L", "C"),
                     help="measurement mode: the 4x-extension head layout prefilled in chunks of C "
                          "tokens up to L against the cache (one G per chunk from its total length)")
+    ap.add_argument("--profile-three-pass", type=int, default=0, metavar="L",
+                    help="A/B mode: single-pass vs three-pass prefill at sequence length L")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                     help="profiling mode: only the prefill of the 4x-extension head layout at "
                          "sequence length L (G from L), warm-up + steps calls; prints timings")
@@ -550,6 +608,8 @@ def main():
         return run_reference(args)
     if args.profile_prefill:
         return run_profile_prefill(args)
+    if args.profile_three_pass:
+        return run_profile_three_pass(args)
     if args.profile_decode:
         return run_profile_decode(args)
     if args.profile_chunked:

@@ -19,6 +19,7 @@ __all__ = [
     "decode_workspace_size",
     "prefill",
     "prefill_chunk",
+    "prefill_three_pass",
     "decode",
     "decode_varlen",
     "device_status",
@@ -92,6 +93,31 @@ def prefill(q, k, v, w0: int, w_pretrained: int, rope_theta: float, softmax_scal
     check(load().jl_bifocal_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq, Hkv, d, int(w0),
         int(w_pretrained), float(rope_theta), float(softmax_scale), _ptr(k_rot_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def prefill_three_pass(q, k, v, w0: int, w_pretrained: int, rope_theta: float, softmax_scale: float = 0.0,
+                       *, out=None, lse=None, want_lse: bool = True, workspace=None, stream=None):
+    """The same prefill in its three-pass inclusion-exclusion form (two window
+    passes and one full aliased pass, merged).  Same arguments and outputs as
+    prefill (no k_rot_out)."""
+    torch = _torch()
+    _need_cuda_bf16("q", q, 4)
+    _need_cuda_bf16("k", k, 4)
+    _need_cuda_bf16("v", v, 4)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(load().jl_bifocal_prefill_three_pass_workspace_size(
+            B, L, Hq, Hkv, d, int(w_pretrained)), q.device)
+    check(load().jl_bifocal_prefill_three_pass(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq, Hkv, d, int(w0),
+        int(w_pretrained), float(rope_theta), float(softmax_scale),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, lse
 

@@ -74,7 +74,7 @@ size_t jl_bifocal_prefill_workspace_size(int B, int L, int Hq, int Hkv, int d, i
   const bool bif = jl::group_size(L, w_pretrained) > 1;
   const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * L * d * 2);
   const size_t kbytes = align_up(static_cast<size_t>(B) * Hkv * L * d * 2);
-  return (bif ? 2 : 1) * (qbytes + kbytes);
+  return (bif ? 2 : 1) * (qbytes + kbytes) + align_up(rope_table_bytes(d));
 }
 
 namespace {
@@ -87,6 +87,8 @@ int check_prefill_shape(const char* who, int B, int L, int Hq, int Hkv, int d, i
   if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "%s: Hq %% Hkv != 0 (%d, %d)", who, Hq, Hkv);
   if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "%s: need w0 >= 0, w_pretrained >= 1", who);
   if (d != 64 && d != 128) return fail(JL_ERR_UNSUPPORTED, "%s: head dim %d (supported: 64, 128)", who, d);
+  if (L > kMaxRopePosition)
+    return fail(JL_ERR_UNSUPPORTED, "%s: positions up to 2^30 - 1 are supported (L = %d)", who, L);
   return JL_OK;
 }
 
@@ -97,9 +99,10 @@ int check_workspace(const char* who, const void* ws, size_t bytes, size_t need) 
   return JL_OK;
 }
 
-// Workspace carving: Q_abs, K_abs, then (G > 1) Q_rem, K_rem.
+// Workspace carving: Q_abs, K_abs, then (G > 1) Q_rem, K_rem, then the
+// rotation tables.
 struct PrefillWs {
-  unsigned char *qa, *ka, *qr, *kr;
+  unsigned char *qa, *ka, *qr, *kr, *tables;
 };
 PrefillWs carve(const void* workspace, int B, int L, int Hq, int Hkv, int d, bool bif) {
   auto* ws = static_cast<unsigned char*>(const_cast<void*>(workspace));
@@ -110,6 +113,7 @@ PrefillWs carve(const void* workspace, int B, int L, int Hq, int Hkv, int d, boo
   w.ka = ws + qbytes;
   w.qr = bif ? ws + qbytes + kbytes : w.qa;
   w.kr = bif ? ws + 2 * qbytes + kbytes : w.ka;
+  w.tables = ws + (bif ? 2 : 1) * (qbytes + kbytes);
   return w;
 }
 
@@ -134,10 +138,12 @@ int jl_bifocal_rope(const void* q, const void* k, int B, int L, int Hq, int Hkv,
   auto stream = static_cast<cudaStream_t>(cuda_stream);
   const RopeFreqs fr = make_rope_freqs(d, rope_theta);
   const TensorView none{nullptr, 0, 0, 0, 0};
-  cudaError_t e = launch_rope_prepass(q, B, L, Hq, d, G, 0, fr, head_major(w.qa, Hq, L, d),
-                                      bif ? head_major(w.qr, Hq, L, d) : none, none, stream);
+  cudaError_t e = launch_rope_tables(w.tables, d, fr, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope: rotation tables");
+  e = launch_rope_prepass(q, B, L, Hq, d, G, 0, w.tables, head_major(w.qa, Hq, L, d),
+                          bif ? head_major(w.qr, Hq, L, d) : none, none, stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (Q)");
-  e = launch_rope_prepass(k, B, L, Hkv, d, G, 0, fr, head_major(w.ka, Hkv, L, d),
+  e = launch_rope_prepass(k, B, L, Hkv, d, G, 0, w.tables, head_major(w.ka, Hkv, L, d),
                           bif ? head_major(w.kr, Hkv, L, d) : none,
                           k_rot_out ? cache_layout(k_rot_out, L, Hkv, d, L) : none, stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope: pre-pass (K)");
@@ -189,6 +195,69 @@ int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, flo
                               workspace, workspace_bytes, cuda_stream);
 }
 
+size_t jl_bifocal_prefill_three_pass_workspace_size(int B, int L, int Hq, int Hkv, int d,
+                                                    int w_pretrained) {
+  const size_t base = jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained);
+  if (base == 0) return 0;
+  const size_t obytes = align_up(static_cast<size_t>(B) * L * Hq * d * 2);
+  const size_t lbytes = align_up(static_cast<size_t>(B) * Hq * L * sizeof(float));
+  return base + 2 * obytes + 3 * lbytes;
+}
+
+int jl_bifocal_prefill_three_pass(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  int B, int L, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                                  double rope_theta, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q || !k || !v || !o) return fail(JL_ERR_INVALID, "three_pass: null q/k/v/o pointer");
+  int rc = check_prefill_shape("three_pass", B, L, Hq, Hkv, d, w0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return fail(JL_ERR_INVALID, "three_pass: every pointer must be 16-byte aligned");
+  rc = check_workspace("three_pass", workspace, workspace_bytes,
+                       jl_bifocal_prefill_three_pass_workspace_size(B, L, Hq, Hkv, d, w_pretrained));
+  if (rc != JL_OK) return rc;
+  rc = jl_bifocal_rope(q, k, B, L, Hq, Hkv, d, w_pretrained, rope_theta, nullptr, workspace,
+                       workspace_bytes, cuda_stream);
+  if (rc != JL_OK) return rc;
+  auto stream = static_cast<cudaStream_t>(cuda_stream);
+  const int G = static_cast<int>(jl::group_size(L, w_pretrained));
+  const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, G > 1);
+  auto* extra = static_cast<unsigned char*>(workspace) +
+                jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained);
+  const size_t obytes = align_up(static_cast<size_t>(B) * L * Hq * d * 2);
+  const size_t lbytes = align_up(static_cast<size_t>(B) * Hq * L * sizeof(float));
+  void* o_a = extra;
+  void* o_c = extra + obytes;
+  float* lse_a = reinterpret_cast<float*>(extra + 2 * obytes);
+  float* lse_b = reinterpret_cast<float*>(extra + 2 * obytes + lbytes);
+  float* lse_c = reinterpret_cast<float*>(extra + 2 * obytes + 2 * lbytes);
+
+  PrefillArgs a;
+  a.v = cache_layout(v, L, Hkv, d, L);
+  a.B = B; a.Lq = L; a.Lk = L; a.q_base = 0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.G = G;
+  a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+  const TensorView q_abs = head_major(w.qa, Hq, L, d), q_rem = head_major(w.qr, Hq, L, d);
+  const TensorView k_abs = head_major(w.ka, Hkv, L, d), k_rem = head_major(w.kr, Hkv, L, d);
+  // A: local window, absolute rotations.
+  a.qa = a.qr = q_abs; a.ka = a.kr = k_abs;
+  a.w0 = w0; a.window_only = true; a.o = o_a; a.lse = lse_a;
+  cudaError_t e = launch_prefill_attention(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "three_pass: pass A");
+  // B: every causal key, aliased rotations (w0 = L: all pairs in one phase).
+  a.qa = a.qr = q_rem; a.ka = a.kr = k_rem;
+  a.w0 = L; a.window_only = false; a.o = o; a.lse = lse_b;
+  e = launch_prefill_attention(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "three_pass: pass B");
+  // C: local window, aliased rotations.
+  a.w0 = w0; a.window_only = true; a.o = o_c; a.lse = lse_c;
+  e = launch_prefill_attention(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "three_pass: pass C");
+  e = launch_three_pass_merge(o_a, lse_a, o, lse_b, o_c, lse_c, lse, B, L, Hq, d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "three_pass: merge");
+  return JL_OK;
+}
+
 size_t jl_bifocal_prefill_chunk_workspace_size(int B, int C, int P0, int Hq, int Hkv, int d,
                                                int w_pretrained) {
   if (B < 1 || C < 1 || P0 < 0 || Hq < 1 || Hkv < 1 || d < 1 || w_pretrained < 1) return 0;
@@ -196,7 +265,7 @@ size_t jl_bifocal_prefill_chunk_workspace_size(int B, int C, int P0, int Hq, int
   const bool bif = jl::group_size(Lk, w_pretrained) > 1;
   const size_t qbytes = align_up(static_cast<size_t>(B) * Hq * C * d * 2);
   const size_t krbytes = align_up(static_cast<size_t>(B) * Hkv * Lk * d * 2);
-  return (bif ? 2 : 1) * qbytes + (bif ? krbytes : 0);
+  return (bif ? 2 : 1) * qbytes + (bif ? krbytes : 0) + align_up(rope_table_bytes(d));
 }
 
 int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
@@ -209,6 +278,8 @@ int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v, void* 
   if (C < 1 || P0 < 0) return fail(JL_ERR_INVALID, "prefill_chunk: need C >= 1 and P0 >= 0");
   if (static_cast<long long>(P0) + C > Lcap)
     return fail(JL_ERR_INVALID, "prefill_chunk: P0 + C = %lld exceeds Lcap = %d", static_cast<long long>(P0) + C, Lcap);
+  if (static_cast<long long>(P0) + C > kMaxRopePosition)
+    return fail(JL_ERR_UNSUPPORTED, "prefill_chunk: positions up to 2^30 - 1 are supported");
   int rc = check_prefill_shape("prefill_chunk", B, C, Hq, Hkv, d, w0, w_pretrained);
   if (rc != JL_OK) return rc;
   if (!(rope_theta > 0.0) || !isfinite(rope_theta))
@@ -227,13 +298,17 @@ int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v, void* 
   void* qa = ws;
   void* qr = bif ? ws + qbytes : qa;
   void* kr = bif ? ws + 2 * qbytes : nullptr;
+  const size_t krbytes = align_up(static_cast<size_t>(B) * Hkv * Lk * d * 2);
+  void* tables = ws + (bif ? 2 * qbytes + krbytes : qbytes);
   auto stream = static_cast<cudaStream_t>(cuda_stream);
   const RopeFreqs fr = make_rope_freqs(d, rope_theta);
+  cudaError_t e = launch_rope_tables(tables, d, fr, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: rotation tables");
   const TensorView none{nullptr, 0, 0, 0, 0};
   const size_t row_elems = static_cast<size_t>(Hkv) * d;
   auto* kc = static_cast<__nv_bfloat16_raw*>(k_cache);
   // 1. Queries at positions P0 .. P0+C-1, both rotations.
-  cudaError_t e = launch_rope_prepass(q, B, C, Hq, d, G, P0, fr, head_major(qa, Hq, C, d),
+  e = launch_rope_prepass(q, B, C, Hq, d, G, P0, tables, head_major(qa, Hq, C, d),
                                       bif ? head_major(qr, Hq, C, d) : none, none, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: pre-pass (Q)");
   // 2. New keys: absolute rotation appended to the cache, aliased rotation
@@ -242,11 +317,11 @@ int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v, void* 
   TensorView kr_new = kr_all;
   if (bif) kr_new.base = static_cast<const unsigned char*>(kr) + static_cast<size_t>(P0) * d * 2;
   TensorView kc_new = cache_layout(kc + static_cast<size_t>(P0) * row_elems, Lcap, Hkv, d, C);
-  e = launch_rope_prepass(k, B, C, Hkv, d, G, P0, fr, none, kr_new, kc_new, stream);
+  e = launch_rope_prepass(k, B, C, Hkv, d, G, P0, tables, none, kr_new, kc_new, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: pre-pass (K)");
   // 3. Cached keys 0 .. P0-1: aliased rotation by the correction R_{f(k)-k}.
   if (bif && P0 > 0) {
-    e = launch_rope_correct(k_cache, B, P0, Lcap, Hkv, d, G, fr, kr_all, stream);
+    e = launch_rope_correct(k_cache, B, P0, Lcap, Hkv, d, G, tables, kr_all, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill_chunk: correction pass");
   }
   // 4. New values appended to the value cache.

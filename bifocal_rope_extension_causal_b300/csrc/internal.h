@@ -33,19 +33,29 @@ inline TensorView cache_layout(const void* base, int Lcap, int H, int d, int row
 }
 
 // ---- RoPE pre-pass (rope_prepass.cu) ---------------------------------------
+// Rotation tables: rows 0..1023 hold R_j, rows 1024..2047 R_{j 2^10}, rows
+// 2048..3071 R_{j 2^20} (positions below 2^30), each row d/2 float4
+// {cos hi, cos lo, sin hi, sin lo}.  Built per call into caller workspace.
+constexpr int kRopeTableRows = 3 * 1024;
+constexpr int kMaxRopePosition = (1 << 30) - 1;
+inline size_t rope_table_bytes(int d) { return static_cast<size_t>(kRopeTableRows) * (d / 2) * 16; }
+cudaError_t launch_rope_tables(void* tables, int d, const RopeFreqs& freqs, cudaStream_t stream);
+
 // Rotates x [B, C, H, d] (raw; row p is position pos0 + p) at the absolute
 // positions into `abs` and at the aliased positions f(pos) = pos / G into
 // `rem`, also writing the absolute rotation into `cache` (rows p of each
-// view; a view with a null base is skipped).
+// view; a view with a null base is skipped).  Every element is the exact
+// rotation rounded to bf16; `tables` come from launch_rope_tables.
 cudaError_t launch_rope_prepass(const void* x, int B, int C, int H, int d, int G, int pos0,
-                                const RopeFreqs& freqs, TensorView abs, TensorView rem,
+                                const void* tables, TensorView abs, TensorView rem,
                                 TensorView cache, cudaStream_t stream);
 
 // Turns keys already rotated at their absolute positions k (cache [B, Lcap,
 // H, d], rows 0 .. P0-1) into keys rotated at f(k) = k / G by the
-// correction rotation R_{f(k) - k}; writes rows 0 .. P0-1 of `rem`.
+// correction rotation R_{f(k) - k}; writes rows 0 .. P0-1 of `rem`
+// (exactly rounded, as above).
 cudaError_t launch_rope_correct(const void* k_cache, int B, int P0, int Lcap, int H, int d, int G,
-                                const RopeFreqs& freqs, TensorView rem, cudaStream_t stream);
+                                const void* tables, TensorView rem, cudaStream_t stream);
 
 // ---- Prefill attention over pre-rotated operands (prefill_tc.cu) -------------
 // Query rows 0 .. Lq-1 sit at positions q_base .. q_base+Lq-1 and attend
@@ -58,8 +68,19 @@ struct PrefillArgs {
   float* lse;         // fp32 [B, Hq, Lq] or nullptr
   int B, Lq, Lk, q_base, Hq, Hkv, d, w0, G;
   float scale_log2;   // softmax scale * log2(e)
+  // Window-only mode (the local views of the three-pass form): score only
+  // the pairs with 0 <= q - k <= w0, with the qa/ka rotations.
+  bool window_only = false;
 };
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+
+// ---- Three-pass merge (three_pass.cu) ----------------------------------------
+// o = (wA oA + wB o - wC oC) / (wA + wB - wC), w_X = exp(lse_X - max(lse_A, lse_B)),
+// in place on o ([B, L, Hq, d] bf16); lse_out [B, Hq, L] (nullable) gets the
+// merged log-sum-exp.
+cudaError_t launch_three_pass_merge(const void* o_a, const float* lse_a, void* o, const float* lse_b,
+                                    const void* o_c, const float* lse_c, float* lse_out, int B, int L,
+                                    int Hq, int d, cudaStream_t stream);
 
 // ---- Decode (decode.cu) ------------------------------------------------------
 struct DecodeArgs {

@@ -13,7 +13,9 @@
 // rotation and only straddling tiles pay for two score sets.  The online
 // softmax makes the order of visits irrelevant.  Only one rotation of Q is
 // resident at a time: after the last remote visit the Q tiles are reloaded
-// with the absolute rotation.
+// with the absolute rotation.  In window-only mode (the local views A and C
+// of the three-pass form, Eq. 7) the remote phase is skipped, and the qa/ka
+// operands are whichever rotation the caller passes.
 //
 // Roles (10 warps):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
@@ -34,6 +36,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "positions.cuh"
@@ -67,6 +71,7 @@ struct Cfg {
 
 struct TcParams {
   int B, Lq, q_base, Hq, Hkv, w0, G, npairs;
+  int window_only;  // skip the remote phase (local views of the three-pass form)
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -80,13 +85,13 @@ struct Plan {
 };
 
 // q0: position of the CTA's first query row; qend: one past the last query
-// position of the call.
-__device__ __forceinline__ Plan make_plan(int q0, int qend, int w0) {
+// position of the call.  window_only: no remote visits.
+__device__ __forceinline__ Plan make_plan(int q0, int qend, int w0, bool window_only) {
   Plan p;
   const int qlast = min(q0 + 2 * kBM - 1, qend - 1);
   p.jmax = qlast / kBN;
   const int t = qlast - w0 - 1;  // remote pairs with key tile j iff kBN * j <= t
-  p.nr = t >= 0 ? min(t / kBN, p.jmax) + 1 : 0;
+  p.nr = (t >= 0 && !window_only) ? min(t / kBN, p.jmax) + 1 : 0;
   const int u = q0 - (kBN - 1) - w0;  // local pairs with key tile j iff kBN * j >= u
   p.jl0 = u <= 0 ? 0 : (u + kBN - 1) / kBN;
   p.nv = p.nr + (p.jmax - p.jl0 + 1);
@@ -129,7 +134,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
   const int hk = h / (prm.Hq / prm.Hkv);
   const int row0 = pair * 2 * kBM;        // first query row of the CTA (local)
   const int q0 = prm.q_base + row0;       // its position
-  const Plan plan = make_plan(q0, prm.q_base + prm.Lq, prm.w0);
+  const Plan plan = make_plan(q0, prm.q_base + prm.Lq, prm.w0, prm.window_only != 0);
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -436,7 +441,10 @@ cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   // One G for the call; with G == 1 both rotations coincide, so every pair
   // is scored in the local phase (no window).
-  p.w0 = (a.G == 1 || a.w0 >= a.Lk) ? (1 << 30) : a.w0;
+  // A window-only call keeps its window (clamped so that position
+  // arithmetic cannot overflow).
+  p.w0 = a.window_only ? std::min(a.w0, 1 << 30) : ((a.G == 1 || a.w0 >= a.Lk) ? (1 << 30) : a.w0);
+  p.window_only = a.window_only ? 1 : 0;
   p.G = a.G;
   p.npairs = (a.Lq + 2 * kBM - 1) / (2 * kBM);
   p.scale_log2 = a.scale_log2;

@@ -55,9 +55,14 @@ extern "C" {
 int64_t jl_group_size(int64_t L, int64_t w_pretrained);
 
 /*
- * Bytes of device workspace jl_bifocal_prefill needs for these sizes
- * (rotated copies of Q and K at absolute and aliased positions; the
- * aliased copies are omitted when G == 1).  Returns 0 for invalid sizes.
+ * Bytes of device workspace jl_bifocal_prefill needs for these sizes.
+ * Returns 0 for invalid sizes.  Layout after jl_bifocal_rope, each part
+ * starting on a 256-byte boundary: Q_abs bf16 [B, Hq, L, d], K_abs bf16
+ * [B, Hkv, L, d], then (only when G > 1) Q_rem [B, Hq, L, d] and K_rem
+ * [B, Hkv, L, d], then the per-call rotation tables (3 * 1024 * d/2 float4).
+ * Every rotated element is the exact rotation R_p x (p = the absolute or the
+ * aliased position) rounded to bf16, round to nearest even.  Positions are
+ * supported up to 2^30 - 1.
  */
 size_t jl_bifocal_prefill_workspace_size(int B, int L, int Hq, int Hkv, int d,
                                          int w_pretrained);
@@ -151,6 +156,34 @@ int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v,
                              float softmax_scale,
                              void* workspace, size_t workspace_bytes,
                              void* cuda_stream);
+
+/*
+ * Three-pass form of the same prefill (digest page, "Method", Eq. 7), kept
+ * as an A/B counterpart of the routed single pass: three causal attention
+ * passes over the pre-rotated operands,
+ *   A  the local window (0 <= q - k <= w0) at absolute rotations,
+ *   B  every causal key at aliased rotations (written into o / a private lse),
+ *   C  the local window at aliased rotations,
+ * merged by inclusion-exclusion, o = (e^lA oA + e^lB oB - e^lC oC) /
+ * (e^lA + e^lB - e^lC), lse = log(e^lA + e^lB - e^lC).  Mathematically
+ * identical to jl_bifocal_prefill; numerically, the merge subtracts C's mass
+ * from B's, so its error grows where the local window holds most of the
+ * aliased-rotation mass.  It scores the window pairs three times.
+ *
+ * Arguments, layouts and errors as jl_bifocal_prefill (no k_rot_out);
+ * workspace >= jl_bifocal_prefill_three_pass_workspace_size(...) bytes, which
+ * holds the rotated operands, oA, oC and the three log-sum-exps.
+ */
+size_t jl_bifocal_prefill_three_pass_workspace_size(int B, int L, int Hq, int Hkv, int d,
+                                                    int w_pretrained);
+
+int jl_bifocal_prefill_three_pass(const void* q, const void* k, const void* v,
+                                  void* o, float* lse,
+                                  int B, int L, int Hq, int Hkv, int d,
+                                  int w0, int w_pretrained, double rope_theta,
+                                  float softmax_scale,
+                                  void* workspace, size_t workspace_bytes,
+                                  void* cuda_stream);
 
 /*
  * Bytes of device workspace jl_bifocal_decode needs (per-split partial

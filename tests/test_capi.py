@@ -59,11 +59,15 @@ def test_group_size_matches_brute_force(lib):
 
 
 def test_workspace_sizes(lib):
-    # G == 1 needs only the absolute copies; G > 1 both.
+    # G == 1 needs only the absolute copies; G > 1 both; plus the rotation
+    # tables (3 * 1024 rows of d/2 float4).
+    tables = 3 * 1024 * 64 * 16
     one = jl.prefill_workspace_size(1, 1024, 4, 2, 128, 4096)
     two = jl.prefill_workspace_size(1, 1024, 4, 2, 128, 512)
-    assert one == 1024 * (4 + 2) * 128 * 2
-    assert two == 2 * one
+    assert one == 1024 * (4 + 2) * 128 * 2 + tables
+    assert two == 2 * (one - tables) + tables
+    three = lib.jl_bifocal_prefill_three_pass_workspace_size(1, 1024, 4, 2, 128, 512)
+    assert three == two + 2 * 1024 * 4 * 128 * 2 + 3 * 4 * 1024 * 4
     assert jl.prefill_workspace_size(0, 1, 1, 1, 64, 1) == 0
     assert jl.decode_workspace_size(1, 32, 128, 131072) > 0
     assert jl.decode_workspace_size(1, 0, 128, 1) == 0

@@ -114,3 +114,29 @@ def test_decode_varlen_flags_bad_lengths(jl):
     with pytest.raises(JetLongError):
         jl.device_status()
     jl.device_status()  # cleared
+
+
+def test_decode_in_cuda_graph(jl):
+    """A decode step captured in a CUDA graph (the serving form: no host work
+    per step) replays to the eager result."""
+    import torch
+    kc, vc, qs = synth.decode_inputs(3000, 8, 2, 128, 77, 1)
+    kc, vc, q = kc.cuda(), vc.cuda(), qs[0].cuda()
+    o_ref, l_ref = jl.decode(q, kc, vc, 2500, 100, 1000, 1e4)
+    o = torch.empty_like(o_ref)
+    lse = torch.empty_like(l_ref)
+    ws = jl.alloc_workspace(jl.decode_workspace_size(1, 8, 128, 3000), q.device)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        jl.decode(q, kc, vc, 2500, 100, 1000, 1e4, out=o, lse=lse, workspace=ws)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        jl.decode(q, kc, vc, 2500, 100, 1000, 1e4, out=o, lse=lse, workspace=ws)
+    o.zero_()
+    lse.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    jl.device_status()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)

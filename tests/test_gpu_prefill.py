@@ -86,14 +86,53 @@ def test_batch_of_two(jl):
 
 
 def test_k_rot_out_is_the_absolute_rotation(jl):
-    """k_rot_out holds R_k x_k (the cache form), within one bf16 rounding."""
+    """k_rot_out holds R_k x_k (the cache form): exactly the oracle's rotation
+    rounded to bf16, bit for bit."""
     L, Hq, Hkv, d = 96, 2, 2, 128
     q, k, v = synth.prefill_inputs(L, Hq, Hkv, d, 11)
     _, _, krot = run_gpu(jl, q, k, v, 8, 32, 1e6, k_rot=True)
-    ref = oracle.rope_rotate(k[0].float().numpy(), np.arange(L), 1e6)
-    got = to_np(krot)[0]
-    assert np.abs(got - ref).max() <= 2.0 ** -8 * max(1.0, np.abs(ref).max())
-    assert np.array_equal(got, oracle.round_to_bf16(got))
+    ref = oracle.round_to_bf16(oracle.rope_rotate(k[0].float().numpy(), np.arange(L), 1e6))
+    assert np.array_equal(to_np(krot)[0], ref)
+
+
+@pytest.mark.parametrize("L,Hq,Hkv,d,wp,theta", [
+    (4096, 8, 4, 128, 1024, 1e6),    # G = 4
+    (3000, 4, 2, 64, 700, 1e4),      # G = 5, d = 64
+    (1050000, 1, 1, 64, 300000, 1e6),  # positions past 2^20: all three table levels
+])
+def test_rotated_operands_are_exactly_rounded(jl, L, Hq, Hkv, d, wp, theta):
+    """The rotated operands in the workspace (Q and K at absolute and aliased
+    positions) equal the oracle's exact rotation rounded to bf16, bit for bit:
+    the kernel's rounding decisions are those of the exact values."""
+    import torch
+    q, k, _ = synth.prefill_inputs(L, Hq, Hkv, d, 5)
+    qd, kd = q.cuda(), k.cuda()
+    nbytes = jl.prefill_workspace_size(1, L, Hq, Hkv, d, wp)
+    ws = jl.alloc_workspace(nbytes, "cuda")
+    jl.check(jl.load().jl_bifocal_rope(
+        jl._ptr(qd), jl._ptr(kd), 1, L, Hq, Hkv, d, wp, theta, None, jl._ptr(ws), nbytes,
+        jl._stream_ptr(None)))
+    torch.cuda.synchronize()
+    G = jl.group_size(L, wp)
+    assert G > 1
+
+    def part(off, H):
+        n = H * L * d * 2
+        t = ws[off:off + n].view(torch.bfloat16).view(H, L, d)
+        return to_np(t), off + (n + 255) // 256 * 256
+
+    qa, off = part(0, Hq)
+    ka, off = part(off, Hkv)
+    qr, off = part(off, Hq)
+    kr, off = part(off, Hkv)
+    pos = np.arange(L)
+    fpos = pos // G
+    for name, got, x, p in (("Q_abs", qa, q, pos), ("K_abs", ka, k, pos), ("Q_rem", qr, q, fpos),
+                            ("K_rem", kr, k, fpos)):
+        xs = x[0].float().numpy()  # [L, H, d]
+        ref = oracle.round_to_bf16(oracle.rope_rotate(xs, p, theta)).transpose(1, 0, 2)
+        bad = int((got != ref).sum())
+        assert bad == 0, f"{name}: {bad} of {ref.size} elements differ from the exactly rounded rotation"
 
 
 def test_values_one_gives_ones(jl):
