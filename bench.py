@@ -38,7 +38,7 @@ from bifocal_rope_extension_causal_b300 import workloads as W  # noqa: E402
 METRIC = "bifocal prefill TFLOP/s & % bf16 tensor peak at 128K; decode HBM GB/s"
 PREFILL = W.EXT_128K
 DECODE = W.DECODE
-KERNELS_PER_PREFILL = 3   # RoPE (Q), RoPE (K), attention
+KERNELS_PER_PREFILL = 4   # rotation tables, RoPE (Q), RoPE (K), attention
 KERNELS_PER_DECODE = 2    # split-K partials, merge
 
 
