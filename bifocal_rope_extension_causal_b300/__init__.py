@@ -20,6 +20,7 @@ __all__ = [
     "prefill",
     "prefill_chunk",
     "prefill_three_pass",
+    "prefill_host",
     "decode",
     "decode_varlen",
     "device_status",
@@ -119,6 +120,45 @@ def prefill_three_pass(q, k, v, w0: int, w_pretrained: int, rope_theta: float, s
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq, Hkv, d, int(w0),
         int(w_pretrained), float(rope_theta), float(softmax_scale),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def _need_host_bf16(name, t, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU tensor (page-locked for overlapped copies)")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor, got shape {tuple(t.shape)}")
+
+
+def prefill_host(q, k, v, w0: int, w_pretrained: int, rope_theta: float, softmax_scale: float = 0.0,
+                 *, out=None, lse=None, want_lse: bool = True, n_chunks: int = 0, workspace=None,
+                 device=None, stream=None):
+    """Prefill from host buffers: q [B, L, Hq, d], k/v [B, L, Hkv, d] bf16 CPU
+    tensors (pinned for overlap).  The library copies chunks in, computes and
+    copies o [B, L, Hq, d] and lse [B, Hq, L] back into host tensors (pinned,
+    allocated if not given).  The outputs are complete after the stream
+    synchronises.  Returns (o, lse)."""
+    torch = _torch()
+    _need_host_bf16("q", q, 4)
+    _need_host_bf16("k", k, 4)
+    _need_host_bf16("v", v, 4)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, L), dtype=torch.float32).pin_memory()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if workspace is None:
+        workspace = alloc_workspace(load().jl_bifocal_prefill_host_workspace_size(
+            B, L, Hq, Hkv, d, int(w_pretrained)), dev)
+    check(load().jl_bifocal_prefill_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq, Hkv, d, int(w0), int(w_pretrained),
+        float(rope_theta), float(softmax_scale), int(n_chunks), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, lse
 
 

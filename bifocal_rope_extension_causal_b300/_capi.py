@@ -63,6 +63,15 @@ SIGNATURES = {
         _c.c_int, _c.c_int, _c.c_double, _c.c_float,       # w0, w_pretrained, theta, scale
         _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
     ]),
+    "jl_bifocal_prefill_host_workspace_size": (_c.c_size_t, [_c.c_int] * 6),
+    "jl_bifocal_prefill_host": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k, v (host)
+        _c.c_void_p, _c.c_void_p,                          # o, lse (host)
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,  # B, L, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_double, _c.c_float,       # w0, w_pretrained, theta, scale
+        _c.c_int,                                          # n_chunks
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_bifocal_decode_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
     "jl_bifocal_decode": (_c.c_int, [
         _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k_cache, v_cache

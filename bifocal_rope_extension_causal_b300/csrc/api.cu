@@ -8,6 +8,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "../../include/jetlong.h"
 #include "internal.h"
@@ -255,6 +256,189 @@ int jl_bifocal_prefill_three_pass(const void* q, const void* k, const void* v, v
   if (e != cudaSuccess) return cuda_fail(e, "three_pass: pass C");
   e = launch_three_pass_merge(o_a, lse_a, o, lse_b, o_c, lse_c, lse, B, L, Hq, d, stream);
   if (e != cudaSuccess) return cuda_fail(e, "three_pass: merge");
+  return JL_OK;
+}
+
+namespace {
+
+// Copy streams and events of the host-buffer prefill, created once per
+// device (the library never allocates device memory).
+constexpr int kPipeEvents = 256;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev[kPipeEvents] = {};
+  int next = 0;
+};
+constexpr int kPipeDevices = 64;
+std::mutex g_pipe_mu;      // creation of the per-device pipes
+std::mutex g_enqueue_mu;   // one host thread at a time enqueues (shares the event pool)
+HostPipe g_pipe[kPipeDevices];
+
+HostPipe* host_pipe(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kPipeDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe& p = g_pipe[dev];
+  if (!p.ready) {
+    if ((*err = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking)) != cudaSuccess) return nullptr;
+    if ((*err = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking)) != cudaSuccess) return nullptr;
+    for (int i = 0; i < kPipeEvents; ++i)
+      if ((*err = cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming)) != cudaSuccess) return nullptr;
+    p.ready = true;
+  }
+  return &p;
+}
+
+// Device buffers of the host-buffer prefill after the prefill workspace:
+// q, k, v, o copies ([B, L, H, d] bf16) and the log-sum-exp staging (chunk c
+// of sequence b as [Hq][rows] at b * Hq * L + c * Hq * C floats).
+struct HostWs {
+  unsigned char *q, *k, *v, *o;
+  float* lse;
+};
+HostWs carve_host(void* workspace, int B, int L, int Hq, int Hkv, int d, int w_pretrained) {
+  auto* ws = static_cast<unsigned char*>(workspace) + jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained);
+  const size_t qb = align_up(static_cast<size_t>(B) * L * Hq * d * 2);
+  const size_t kb = align_up(static_cast<size_t>(B) * L * Hkv * d * 2);
+  HostWs h;
+  h.q = ws;
+  h.k = ws + qb;
+  h.v = ws + qb + kb;
+  h.o = ws + qb + 2 * kb;
+  h.lse = reinterpret_cast<float*>(ws + 2 * qb + 2 * kb);
+  return h;
+}
+
+TensorView rows_of(TensorView t, int r0, int rows, int d) {
+  t.base = static_cast<const unsigned char*>(t.base) + static_cast<size_t>(r0) * d * 2;
+  t.rows = rows;
+  return t;
+}
+
+}  // namespace
+
+size_t jl_bifocal_prefill_host_workspace_size(int B, int L, int Hq, int Hkv, int d, int w_pretrained) {
+  const size_t base = jl_bifocal_prefill_workspace_size(B, L, Hq, Hkv, d, w_pretrained);
+  if (base == 0) return 0;
+  const size_t qb = align_up(static_cast<size_t>(B) * L * Hq * d * 2);
+  const size_t kb = align_up(static_cast<size_t>(B) * L * Hkv * d * 2);
+  return base + 2 * qb + 2 * kb + align_up(static_cast<size_t>(B) * Hq * L * sizeof(float));
+}
+
+int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            float* lse_host, int B, int L, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                            double rope_theta, float softmax_scale, int n_chunks, void* workspace,
+                            size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (!q_host || !k_host || !v_host || !o_host) return fail(JL_ERR_INVALID, "prefill_host: null q/k/v/o pointer");
+  int rc = check_prefill_shape("prefill_host", B, L, Hq, Hkv, d, w0, w_pretrained);
+  if (rc != JL_OK) return rc;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "prefill_host: rope_theta must be > 0");
+  if (n_chunks < 0) return fail(JL_ERR_INVALID, "prefill_host: n_chunks must be >= 0");
+  rc = check_workspace("prefill_host", workspace, workspace_bytes,
+                       jl_bifocal_prefill_host_workspace_size(B, L, Hq, Hkv, d, w_pretrained));
+  if (rc != JL_OK) return rc;
+  cudaError_t e = cudaSuccess;
+  HostPipe* pipe = host_pipe(&e);
+  if (pipe == nullptr) return cuda_fail(e, "prefill_host: copy streams");
+  auto stream = static_cast<cudaStream_t>(cuda_stream);
+  std::lock_guard<std::mutex> lock(g_enqueue_mu);
+  auto event = [&]() {
+    cudaEvent_t ev = pipe->ev[pipe->next];
+    pipe->next = (pipe->next + 1) % kPipeEvents;
+    return ev;
+  };
+  // Query chunks of C rows, C a multiple of 256 (the attention kernel's
+  // query-tile pair), so each chunk's tiles are those of a single call.
+  const int nc_req = n_chunks > 0 ? n_chunks : std::min(16, std::max(1, L / 16384));
+  int C = (L + nc_req - 1) / nc_req;
+  C = (C + 255) / 256 * 256;
+  const int nc = (L + C - 1) / C;
+
+  const int G = static_cast<int>(jl::group_size(L, w_pretrained));
+  const bool bif = G > 1;
+  const PrefillWs w = carve(workspace, B, L, Hq, Hkv, d, bif);
+  const HostWs h = carve_host(workspace, B, L, Hq, Hkv, d, w_pretrained);
+  const RopeFreqs fr = make_rope_freqs(d, rope_theta);
+  const TensorView none{nullptr, 0, 0, 0, 0};
+  const size_t qrow = static_cast<size_t>(Hq) * d * 2, krow = static_cast<size_t>(Hkv) * d * 2;
+  const float scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+
+  // The copy streams start after the work already queued on the caller's stream.
+  cudaEvent_t ev = event();
+  if ((e = cudaEventRecord(ev, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: event");
+  cudaStreamWaitEvent(pipe->h2d, ev, 0);
+  cudaStreamWaitEvent(pipe->d2h, ev, 0);
+  if ((e = launch_rope_tables(w.tables, d, fr, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: tables");
+  for (int b = 0; b < B; ++b) {
+    const size_t qoff = static_cast<size_t>(b) * L * qrow, koff = static_cast<size_t>(b) * L * krow;
+    const TensorView qa = head_major(w.qa + static_cast<size_t>(b) * Hq * L * d * 2, Hq, L, d);
+    const TensorView qr = head_major(w.qr + static_cast<size_t>(b) * Hq * L * d * 2, Hq, L, d);
+    const TensorView ka = head_major(w.ka + static_cast<size_t>(b) * Hkv * L * d * 2, Hkv, L, d);
+    const TensorView kr = head_major(w.kr + static_cast<size_t>(b) * Hkv * L * d * 2, Hkv, L, d);
+    for (int c = 0; c < nc; ++c) {
+      const int r0 = c * C, rows = std::min(C, L - r0);
+      // 1. Chunk rows of q, k, v in.
+      const size_t qo = qoff + static_cast<size_t>(r0) * qrow, ko = koff + static_cast<size_t>(r0) * krow;
+      e = cudaMemcpyAsync(h.q + qo, static_cast<const unsigned char*>(q_host) + qo, rows * qrow,
+                          cudaMemcpyHostToDevice, pipe->h2d);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h.k + ko, static_cast<const unsigned char*>(k_host) + ko, rows * krow,
+                            cudaMemcpyHostToDevice, pipe->h2d);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h.v + ko, static_cast<const unsigned char*>(v_host) + ko, rows * krow,
+                            cudaMemcpyHostToDevice, pipe->h2d);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: copy in");
+      ev = event();
+      cudaEventRecord(ev, pipe->h2d);
+      cudaStreamWaitEvent(stream, ev, 0);
+      // 2. Rotations of the chunk's rows (the call's G).
+      e = launch_rope_prepass(h.q + qo, 1, rows, Hq, d, G, r0, w.tables, rows_of(qa, r0, rows, d),
+                              bif ? rows_of(qr, r0, rows, d) : none, none, stream);
+      if (e == cudaSuccess)
+        e = launch_rope_prepass(h.k + ko, 1, rows, Hkv, d, G, r0, w.tables, rows_of(ka, r0, rows, d),
+                                bif ? rows_of(kr, r0, rows, d) : none, none, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: pre-pass");
+      // 3. The chunk's query rows over keys 0 .. r0 + rows - 1.
+      PrefillArgs a;
+      a.qa = rows_of(qa, r0, rows, d);
+      a.qr = bif ? rows_of(qr, r0, rows, d) : a.qa;
+      a.ka = rows_of(ka, 0, r0 + rows, d);
+      a.kr = bif ? rows_of(kr, 0, r0 + rows, d) : a.ka;
+      a.v = cache_layout(h.v + koff, L, Hkv, d, r0 + rows);
+      a.o = h.o + qo;
+      float* lse_stage = h.lse + static_cast<size_t>(b) * Hq * L + static_cast<size_t>(c) * Hq * C;
+      a.lse = lse_host ? lse_stage : nullptr;
+      a.B = 1; a.Lq = rows; a.Lk = r0 + rows; a.q_base = r0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
+      a.scale_log2 = scale_log2;
+      if ((e = launch_prefill_attention(a, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: attention");
+      ev = event();
+      cudaEventRecord(ev, stream);
+      cudaStreamWaitEvent(pipe->d2h, ev, 0);
+      // 4. The chunk's outputs out.
+      e = cudaMemcpyAsync(static_cast<unsigned char*>(o_host) + qo, h.o + qo, rows * qrow, cudaMemcpyDeviceToHost,
+                          pipe->d2h);
+      if (e == cudaSuccess && lse_host)
+        e = cudaMemcpy2DAsync(lse_host + static_cast<size_t>(b) * Hq * L + r0, static_cast<size_t>(L) * sizeof(float),
+                              lse_stage, static_cast<size_t>(rows) * sizeof(float), rows * sizeof(float), Hq,
+                              cudaMemcpyDeviceToHost, pipe->d2h);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: copy out");
+    }
+  }
+  // The caller's stream resumes after the last copy out (and the last copy in).
+  ev = event();
+  cudaEventRecord(ev, pipe->d2h);
+  cudaStreamWaitEvent(stream, ev, 0);
+  ev = event();
+  cudaEventRecord(ev, pipe->h2d);
+  cudaStreamWaitEvent(stream, ev, 0);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "prefill_host: stream ordering");
   return JL_OK;
 }
 

@@ -186,6 +186,41 @@ int jl_bifocal_prefill_three_pass(const void* q, const void* k, const void* v,
                                   void* cuda_stream);
 
 /*
+ * The same prefill with q, k, v, o and lse in HOST memory: the library copies
+ * the inputs in and the outputs out itself, pipelined by query chunks so that
+ * the copies overlap the kernels.  Chunk c (rows r0 .. r0 + rows - 1, rows a
+ * multiple of 256 except the last) is copied in on a library copy stream,
+ * rotated, attended over keys 0 .. r0 + rows - 1 with the call's single G,
+ * and its o and lse rows are copied out on a second copy stream while the
+ * next chunk computes.  Results are bit-identical to jl_bifocal_prefill on
+ * the same data.
+ *
+ *  q_host  bf16 [B, L, Hq, d], k_host / v_host bf16 [B, L, Hkv, d]  (read)
+ *  o_host  bf16 [B, L, Hq, d]; lse_host fp32 [B, Hq, L] or NULL       (written)
+ *  n_chunks  query chunks per sequence; 0 picks min(16, max(1, L / 16384))
+ *  workspace >= jl_bifocal_prefill_host_workspace_size(...) bytes (device):
+ *            the prefill workspace plus device copies of q, k, v, o and lse
+ *  other arguments as jl_bifocal_prefill
+ *
+ * Asynchronous on cuda_stream like every call: the host outputs are complete
+ * once the stream has synchronised, and the host buffers must stay valid
+ * until then.  Page-locked host buffers are needed for the copies to overlap;
+ * pageable ones are correct but serialise.  The two copy streams and an
+ * event pool are created on the first call on each device and kept; calls
+ * from several host threads are serialised while they enqueue.
+ */
+size_t jl_bifocal_prefill_host_workspace_size(int B, int L, int Hq, int Hkv, int d,
+                                              int w_pretrained);
+
+int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* v_host,
+                            void* o_host, float* lse_host,
+                            int B, int L, int Hq, int Hkv, int d,
+                            int w0, int w_pretrained, double rope_theta,
+                            float softmax_scale, int n_chunks,
+                            void* workspace, size_t workspace_bytes,
+                            void* cuda_stream);
+
+/*
  * Bytes of device workspace jl_bifocal_decode needs (per-split partial
  * softmax statistics and outputs) for caches of up to Lcap positions.
  * Returns 0 for invalid sizes.
