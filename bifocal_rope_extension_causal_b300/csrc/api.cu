@@ -356,7 +356,7 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
   };
   // Query chunks of C rows, C a multiple of 256 (the attention kernel's
   // query-tile pair), so each chunk's tiles are those of a single call.
-  const int nc_req = n_chunks > 0 ? n_chunks : std::min(16, std::max(1, L / 16384));
+  const int nc_req = n_chunks > 0 ? n_chunks : std::min(16, std::max(1, L / 8192));
   int C = (L + nc_req - 1) / nc_req;
   C = (C + 255) / 256 * 256;
   const int nc = (L + C - 1) / C;

@@ -197,7 +197,7 @@ int jl_bifocal_prefill_three_pass(const void* q, const void* k, const void* v,
  *
  *  q_host  bf16 [B, L, Hq, d], k_host / v_host bf16 [B, L, Hkv, d]  (read)
  *  o_host  bf16 [B, L, Hq, d]; lse_host fp32 [B, Hq, L] or NULL       (written)
- *  n_chunks  query chunks per sequence; 0 picks min(16, max(1, L / 16384))
+ *  n_chunks  query chunks per sequence; 0 picks min(16, max(1, L / 8192))
  *  workspace >= jl_bifocal_prefill_host_workspace_size(...) bytes (device):
  *            the prefill workspace plus device copies of q, k, v, o and lse
  *  other arguments as jl_bifocal_prefill
