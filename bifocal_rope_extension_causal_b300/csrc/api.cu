@@ -375,7 +375,22 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
   if ((e = cudaEventRecord(ev, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: event");
   cudaStreamWaitEvent(pipe->h2d, ev, 0);
   cudaStreamWaitEvent(pipe->d2h, ev, 0);
-  if ((e = launch_rope_tables(w.tables, d, fr, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: tables");
+  // Every exit from here on (errors included) makes the caller's stream wait
+  // for both copy streams, so no copy is still in flight on the workspace or
+  // the host buffers once that stream has synchronised.
+  auto join = [&]() {
+    cudaEvent_t j = event();
+    cudaEventRecord(j, pipe->d2h);
+    cudaStreamWaitEvent(stream, j, 0);
+    j = event();
+    cudaEventRecord(j, pipe->h2d);
+    cudaStreamWaitEvent(stream, j, 0);
+  };
+  auto fail_joined = [&](cudaError_t err, const char* what) {
+    join();
+    return cuda_fail(err, what);
+  };
+  if ((e = launch_rope_tables(w.tables, d, fr, stream)) != cudaSuccess) return fail_joined(e, "prefill_host: tables");
   for (int b = 0; b < B; ++b) {
     const size_t qoff = static_cast<size_t>(b) * L * qrow, koff = static_cast<size_t>(b) * L * krow;
     const TensorView qa = head_major(w.qa + static_cast<size_t>(b) * Hq * L * d * 2, Hq, L, d);
@@ -394,7 +409,7 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
       if (e == cudaSuccess)
         e = cudaMemcpyAsync(h.v + ko, static_cast<const unsigned char*>(v_host) + ko, rows * krow,
                             cudaMemcpyHostToDevice, pipe->h2d);
-      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: copy in");
+      if (e != cudaSuccess) return fail_joined(e, "prefill_host: copy in");
       ev = event();
       cudaEventRecord(ev, pipe->h2d);
       cudaStreamWaitEvent(stream, ev, 0);
@@ -404,7 +419,7 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
       if (e == cudaSuccess)
         e = launch_rope_prepass(h.k + ko, 1, rows, Hkv, d, G, r0, w.tables, rows_of(ka, r0, rows, d),
                                 bif ? rows_of(kr, r0, rows, d) : none, none, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: pre-pass");
+      if (e != cudaSuccess) return fail_joined(e, "prefill_host: pre-pass");
       // 3. The chunk's query rows over keys 0 .. r0 + rows - 1.
       PrefillArgs a;
       a.qa = rows_of(qa, r0, rows, d);
@@ -417,7 +432,7 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
       a.lse = lse_host ? lse_stage : nullptr;
       a.B = 1; a.Lq = rows; a.Lk = r0 + rows; a.q_base = r0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
       a.scale_log2 = scale_log2;
-      if ((e = launch_prefill_attention(a, stream)) != cudaSuccess) return cuda_fail(e, "prefill_host: attention");
+      if ((e = launch_prefill_attention(a, stream)) != cudaSuccess) return fail_joined(e, "prefill_host: attention");
       ev = event();
       cudaEventRecord(ev, stream);
       cudaStreamWaitEvent(pipe->d2h, ev, 0);
@@ -428,16 +443,11 @@ int jl_bifocal_prefill_host(const void* q_host, const void* k_host, const void* 
         e = cudaMemcpy2DAsync(lse_host + static_cast<size_t>(b) * Hq * L + r0, static_cast<size_t>(L) * sizeof(float),
                               lse_stage, static_cast<size_t>(rows) * sizeof(float), rows * sizeof(float), Hq,
                               cudaMemcpyDeviceToHost, pipe->d2h);
-      if (e != cudaSuccess) return cuda_fail(e, "prefill_host: copy out");
+      if (e != cudaSuccess) return fail_joined(e, "prefill_host: copy out");
     }
   }
   // The caller's stream resumes after the last copy out (and the last copy in).
-  ev = event();
-  cudaEventRecord(ev, pipe->d2h);
-  cudaStreamWaitEvent(stream, ev, 0);
-  ev = event();
-  cudaEventRecord(ev, pipe->h2d);
-  cudaStreamWaitEvent(stream, ev, 0);
+  join();
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "prefill_host: stream ordering");
   return JL_OK;
 }
