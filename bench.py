@@ -516,6 +516,49 @@ def run_profile_decode(args):
     return 0
 
 
+def run_profile_decode_varlen(args):
+    """Batched decode with per-sequence lengths: B sequences of the decode
+    workload's head layout, lengths spread over [L/2, L], one call per step
+    (jl_bifocal_decode_varlen), timed as CUDA-graph replays."""
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    dw = DECODE
+    B, L = (int(x) for x in args.profile_decode_varlen)
+    dev = torch.device("cuda", 0)
+    kc, vc, qs = synth.decode_inputs(L, dw.Hq, dw.Hkv, dw.d, dw.index, 1, B=B)
+    kc, vc, q = kc.to(dev), vc.to(dev), qs[0].to(dev)
+    lengths = [L - (L // 2) * i // max(1, B - 1) for i in range(B)]
+    seq = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    ws = jl.alloc_workspace(jl.decode_workspace_size(B, dw.Hq, dw.d, L), dev)
+    o = torch.empty((B, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, dw.Hq), dtype=torch.float32, device=dev)
+    run = lambda: jl.decode_varlen(q, kc, vc, seq, dw.w0, dw.w_pretrained, dw.theta, max_len=L, out=o, lse=lse,
+                                   workspace=ws)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(max(3, args.warmup)):
+            run()
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            run()
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    jl.device_status()
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    nbytes = sum(W.decode_bytes(n, dw.Hkv, dw.d, dw.Hq) for n in lengths)
+    print(json.dumps({"profile_decode_varlen_B": B, "max_len": L, "lengths": lengths, "us": round(us, 2),
+                      "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "tokens_per_s": round(B / (us * 1e-6), 1)}))
+    return 0
+
+
 def run_profile_chunked(args):
     """Chunked prefill of one sequence: every chunk attends to the cache
     filled by the chunks before it.  Reports the per-chunk times and the
@@ -595,6 +638,8 @@ def main():
     ap.add_argument("--profile-chunked", type=int, nargs=2, default=None, metavar=("L", "C"),
                     help="measurement mode: the 4x-extension head layout prefilled in chunks of C "
                          "tokens up to L against the cache (one G per chunk from its total length)")
+    ap.add_argument("--profile-decode-varlen", type=int, nargs=2, default=None, metavar=("B", "L"),
+                    help="profiling mode: batched decode of B sequences, lengths spread over [L/2, L]")
     ap.add_argument("--profile-three-pass", type=int, default=0, metavar="L",
                     help="A/B mode: single-pass vs three-pass prefill at sequence length L")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
@@ -608,6 +653,8 @@ def main():
         return run_profile_prefill(args)
     if args.profile_three_pass:
         return run_profile_three_pass(args)
+    if args.profile_decode_varlen:
+        return run_profile_decode_varlen(args)
     if args.profile_decode:
         return run_profile_decode(args)
     if args.profile_chunked:

@@ -65,6 +65,7 @@ constexpr int kStages = 2;      // per-warp ring depth
 // eight query heads per KV head.
 __host__ __device__ constexpr int warps_per_head(int gq) { return gq <= 4 ? 2 : 1; }
 constexpr int kMaxSplits = 512;
+constexpr int kMinBlocksPerSplit = 8;  // batched decode: blocks per slice when the batch fills the SMs
 constexpr int kStageBytes = kStep * 2 * kD * 2;  // K and V rows of one step
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kTabStride = 36;  // float4 per key row of the rotation table (32 + 4 padding)
@@ -682,9 +683,15 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int Lcap) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.d != kD) return cudaErrorInvalidValue;
   const int GQ = a.Hq / a.Hkv;
+  // Blocks per slice: enough slices for one wave over the SMs for one
+  // sequence; with a batch, up to kMinBlocksPerSplit blocks per slice as long
+  // as the batch's slices still fill a wave (short sequences would otherwise
+  // pay the per-CTA set-up for a single 64-key block).
   const int nblocks = (a.L + kBlockKeys - 1) / kBlockKeys;
   const int target = std::min(num_sms(), kMaxSplits);
-  const int bps = (nblocks + target - 1) / target;
+  const int fill = static_cast<int>(std::min<long long>(kMinBlocksPerSplit,
+                                                         static_cast<long long>(nblocks) * a.B / num_sms()));
+  const int bps = std::max((nblocks + target - 1) / target, fill);
   const int nsplit = (nblocks + bps - 1) / bps;
 
   DecodeKParams p;
