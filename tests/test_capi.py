@@ -99,6 +99,58 @@ def test_prefill_argument_checks(lib, kw, code):
     assert lib.jl_last_error().decode()
 
 
+def _three_pass_args(**kw):
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, lse=None, B=1, L=128, Hq=2, Hkv=1, d=128,
+             w0=16, wp=64, theta=1e4, scale=0.0, ws=1 << 20, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return (a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"], a["Hkv"], a["d"],
+            a["w0"], a["wp"], a["theta"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(v=None), _capi.JL_ERR_INVALID),
+    (dict(Hq=3, Hkv=2), _capi.JL_ERR_INVALID),
+    (dict(d=96), _capi.JL_ERR_UNSUPPORTED),
+    (dict(L=1 << 30), _capi.JL_ERR_UNSUPPORTED),
+    (dict(wsb=1 << 20), _capi.JL_ERR_WORKSPACE),
+])
+def test_three_pass_argument_checks(lib, kw, code):
+    assert lib.jl_bifocal_prefill_three_pass(*_three_pass_args(**kw)) == code
+    assert lib.jl_last_error().decode()
+
+
+def _host_args(**kw):
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, lse=None, B=1, L=128, Hq=2, Hkv=1, d=128,
+             w0=16, wp=64, theta=1e4, scale=0.0, nc=0, ws=1 << 20, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return (a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"], a["Hkv"], a["d"],
+            a["w0"], a["wp"], a["theta"], a["scale"], a["nc"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(o=None), _capi.JL_ERR_INVALID),
+    (dict(nc=-1), _capi.JL_ERR_INVALID),
+    (dict(theta=-1.0), _capi.JL_ERR_INVALID),
+    (dict(B=0), _capi.JL_ERR_INVALID),
+    (dict(d=32), _capi.JL_ERR_UNSUPPORTED),
+    (dict(ws=None), _capi.JL_ERR_WORKSPACE),
+    (dict(wsb=4096), _capi.JL_ERR_WORKSPACE),
+])
+def test_host_prefill_argument_checks(lib, kw, code):
+    """Rejected before any CUDA call (host pointers are never dereferenced here)."""
+    assert lib.jl_bifocal_prefill_host(*_host_args(**kw)) == code
+    assert lib.jl_last_error().decode()
+
+
+def test_host_prefill_workspace_size(lib):
+    base = lib.jl_bifocal_prefill_workspace_size(2, 1000, 4, 2, 128, 300)
+    host = lib.jl_bifocal_prefill_host_workspace_size(2, 1000, 4, 2, 128, 300)
+    def up(x):
+        return (x + 255) // 256 * 256
+    assert host == base + 2 * up(2 * 1000 * 4 * 128 * 2) + 2 * up(2 * 1000 * 2 * 128 * 2) + up(2 * 4 * 1000 * 4)
+    assert lib.jl_bifocal_prefill_host_workspace_size(0, 1000, 4, 2, 128, 300) == 0
+
+
 def _decode_args(**kw):
     a = dict(q=1 << 20, kc=1 << 20, vc=1 << 20, L=10, Lcap=16, o=1 << 20, lse=None, B=1, Hq=4,
              Hkv=2, d=128, w0=4, wp=8, theta=1e4, scale=0.0, ws=1 << 20, wsb=1 << 30, stream=None)
