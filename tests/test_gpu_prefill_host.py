@@ -49,3 +49,16 @@ def test_host_prefill_without_lse_and_repeated(jl):
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(o, o_ref.cpu())
+
+
+def test_host_prefill_pageable_buffers(jl):
+    """Pageable (not page-locked) host tensors: the copies serialise with the
+    host thread, and the results are still those of the device prefill."""
+    import torch
+    q, k, v = synth.prefill_inputs(1500, 4, 2, 128, seed=8)
+    o_ref, l_ref = jl.prefill(q.cuda(), k.cuda(), v.cuda(), 40, 400, 1e4)
+    out = torch.empty(q.shape, dtype=torch.bfloat16)
+    lse = torch.empty((1, 4, 1500), dtype=torch.float32)
+    o, l = jl.prefill_host(q, k, v, 40, 400, 1e4, out=out, lse=lse, n_chunks=3)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref.cpu()) and torch.equal(l, l_ref.cpu())
