@@ -42,6 +42,14 @@ MUTATIONS = [
      "rnd(cached)"),
     ("chunk: query positions from zero", "qpos = np.arange(P0, Lt, dtype=np.int64)",
      "qpos = np.arange(0, C, dtype=np.int64)"),
+    ("GQA heads interleaved", "            for h in range(hk * group, (hk + 1) * group):\n                rh",
+     "            for h in range(hk, Hq, Hkv):\n                rh"),
+    ("three-pass window strict", "window = causal & (dist <= w0)", "window = causal & (dist < w0)"),
+    ("chunk: G from the chunk length", "    G = group_size(Lt, w_pretrained)", "    G = group_size(C, w_pretrained)"),
+    ("decode: remote query at the absolute position", "q_rem = rope_rotate(xq, [alias(qp, G)], theta)[0]",
+     "q_rem = rope_rotate(xq, [qp], theta)[0]"),
+    ("decode: G from the cache capacity", "    G = group_size(L, w_pretrained)\n    if scale is None:\n        scale = 1.0 / math.sqrt(d)\n    qp",
+     "    G = group_size(k_cache.shape[1], w_pretrained)\n    if scale is None:\n        scale = 1.0 / math.sqrt(d)\n    qp"),
 ]
 
 
