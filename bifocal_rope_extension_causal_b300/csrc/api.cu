@@ -545,37 +545,31 @@ size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap) {
 
 }  // extern "C"
 
-namespace {
+namespace jl {
 
 // Validation shared by the decode entry points; L is the (largest) length.
-int check_decode(const char* who, const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
-                 const void* o, int B, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta) {
+int check_decode_args(const char* who, const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
+                      const void* o, int B, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta) {
   if (!q || !k_cache || !v_cache || !o) return fail(JL_ERR_INVALID, "%s: null q/cache/o pointer", who);
   if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1) return fail(JL_ERR_INVALID, "%s: need B, Hq, Hkv, Lcap >= 1", who);
   if (L < 1 || L > Lcap) return fail(JL_ERR_INVALID, "%s: need 1 <= L <= Lcap (got L=%d, Lcap=%d)", who, L, Lcap);
   if (Hq % Hkv != 0) return fail(JL_ERR_INVALID, "%s: Hq %% Hkv != 0 (%d, %d)", who, Hq, Hkv);
   if (w0 < 0 || w_pretrained < 1) return fail(JL_ERR_INVALID, "%s: need w0 >= 0, w_pretrained >= 1", who);
   if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return fail(JL_ERR_INVALID, "%s: rope_theta must be > 0", who);
-  if (d != 128) return fail(JL_ERR_UNSUPPORTED, "%s: head dim %d (supported: 128)", who, d);
-  const int GQ = Hq / Hkv;
-  if (Hkv > 8 || (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8))
-    return fail(JL_ERR_UNSUPPORTED, "%s: need Hkv <= 8 and Hq/Hkv in {1,2,4,8} (got %d, %d)", who, Hkv, GQ);
+  if (d != 64 && d != 128) return fail(JL_ERR_UNSUPPORTED, "%s: head dim %d (supported: 64, 128)", who, d);
+  if (!decode_supported(Hq, Hkv, d))
+    return fail(JL_ERR_UNSUPPORTED, "%s: need 1 <= Hq/Hkv <= 8 query heads per KV head (got %d)", who, Hq / Hkv);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
     return fail(JL_ERR_INVALID, "%s: every pointer must be 16-byte aligned", who);
   return JL_OK;
 }
 
-int run_decode(const char* who, const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
-               int L, int Lcap, void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
-               double rope_theta, float softmax_scale, void* workspace, size_t workspace_bytes,
-               void* cuda_stream) {
-  int rc = check_decode(who, q, k_cache, v_cache, L, Lcap, o, B, Hq, Hkv, d, w0, w_pretrained, rope_theta);
-  if (rc != JL_OK) return rc;
-  rc = check_workspace(who, workspace, workspace_bytes, jl_bifocal_decode_workspace_size(B, Hq, d, Lcap));
-  if (rc != JL_OK) return rc;
+int decode_call(const char* who, const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                int L, int Lcap, void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                double rope_theta, float softmax_scale, float* partials, void* cuda_stream) {
   DecodeArgs a;
   a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.o = o; a.lse = lse;
-  a.part = static_cast<float*>(workspace);
+  a.part = partials;
   a.seqlens = seqlens;
   a.B = B; a.L = L; a.Lcap = Lcap; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0;
   a.G = static_cast<int>(jl::group_size(L, w_pretrained));
@@ -583,8 +577,24 @@ int run_decode(const char* who, const void* q, const void* k_cache, const void* 
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
   a.freqs = make_rope_freqs(d, rope_theta);
   const cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
-  if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
+  if (e != cudaSuccess) return fail(JL_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return JL_OK;
+}
+
+}  // namespace jl
+
+namespace {
+
+int run_decode(const char* who, const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+               int L, int Lcap, void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+               double rope_theta, float softmax_scale, void* workspace, size_t workspace_bytes,
+               void* cuda_stream) {
+  int rc = check_decode_args(who, q, k_cache, v_cache, L, Lcap, o, B, Hq, Hkv, d, w0, w_pretrained, rope_theta);
+  if (rc != JL_OK) return rc;
+  rc = check_workspace(who, workspace, workspace_bytes, jl_bifocal_decode_workspace_size(B, Hq, d, Lcap));
+  if (rc != JL_OK) return rc;
+  return decode_call(who, q, k_cache, v_cache, seqlens, L, Lcap, o, lse, B, Hq, Hkv, d, w0, w_pretrained,
+                     rope_theta, softmax_scale, static_cast<float*>(workspace), cuda_stream);
 }
 
 }  // namespace

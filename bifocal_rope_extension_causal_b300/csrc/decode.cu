@@ -6,44 +6,52 @@
 // Delta_k = f(j) - j, because R_a R_b = R_{a+b} turns R_j x_j into
 // R_{f(j)} x_j, while the query is rotated at f(q) (Delta_q = f(q) - q).
 //
-// Work split.  The key range [0, L) is cut into `nsplit` contiguous slices
-// (whole 64-key blocks), one CTA each, about one per SM; a CTA covers all KV
-// heads of its slice (two warps per KV head), so the per-key rotation table
-// is built once and shared by all heads.  Each CTA writes an unnormalised
+// Work split.  The key range [0, L) is cut into `nsplit` contiguous slices of
+// whole 16-key steps, as even as the step count allows, one CTA each and
+// about one per SM; a CTA covers up to eight KV heads of its slice (more KV
+// heads take more CTAs along grid z), so the per-key rotation table is built
+// once and shared by all of its heads.  Each CTA writes an unnormalised
 // partial (running max m, sum l, sum p v) per query head; a second kernel,
 // launched as a programmatic dependent of the first, merges the slices with
 // log-sum-exp weights.
 //
-// Memory path.  kWarpsPerHead warps per KV head take alternate 8-key steps;
-// each streams its head's K and V rows (256 B each per key) through its own
-// kStages-deep shared-memory ring with 16-byte cp.async copies (16 lanes per
-// row: fully coalesced; keys past the slice end are zero-filled).  The
-// 16-byte chunks of a row are XOR-swizzled by the key index so that the
+// Memory path.  One warp per KV head (more when a CTA holds fewer than
+// eight heads, taking alternate steps) streams the head's K and V rows (2d
+// bytes each per key) through its own two-stage shared-memory ring with
+// 16-byte cp.async copies (fully coalesced; keys past the slice end are
+// zero-filled).  The query rows and both ring stages are requested before
+// any set-up work, so the set-up runs while the first keys are in flight.
+// The 16-byte chunks of a row are XOR-swizzled by the key index so that the
 // 8x8 ldmatrix tiles read below are free of bank conflicts.
 //
-// Arithmetic.  The per-key work runs on the tensor cores (warp-level
-// mma.sync, bf16 operands, fp32 accumulation), which leaves the CUDA cores
-// only the key rotation and the softmax; issue, not HBM, bounds the plain
-// CUDA-core form of this loop.  Precision is kept at fp32 level by splitting
-// every operand that is not already bf16 into bf16 hi + lo parts:
-//   scores (m16n8k16)  A = the step's 8 keys, corrected by R_{Delta_k} in
-//                      fp32 and split (rows 0..7 hi, rows 8..15 lo);
-//                      B = the pre-scaled rotated query heads of the KV
-//                      head as (hi, lo) column pairs.  The four products of
-//                      a (key, head) land in one lane's accumulator.
-//   O += P V (m16n8k8) computed as O^T += V^T P^T: A = V^T from transposed
-//                      ldmatrix tiles, B = P split as hi + lo (with at most
-//                      four query heads per KV head the lo parts fill the
-//                      idle columns 4..7).
-// The softmax runs in the score fragment (one lane per (key, head)) with
-// lazily raised maxima.
+// Arithmetic.  A step is 16 keys of one KV head.  The per-key work runs on
+// the tensor cores (warp-level mma.sync m16n8k16, bf16 operands, fp32
+// accumulation), which leaves the CUDA cores only the key rotation and the
+// softmax.  Precision is kept at fp32 level by splitting every operand that
+// is not already bf16 into bf16 hi + lo parts:
+//   scores   A = the step's 16 keys, corrected by R_{Delta_k} in fp32 and
+//            split: one product with the hi parts, one with the lo parts;
+//            B = the pre-scaled rotated query heads of the KV head as
+//            (hi, lo) column pairs.  The four products of a (key, head) land
+//            in one lane's accumulator.  Local keys are exact in bf16 and
+//            take one product.
+//   O += P V computed as O^T += V^T P^T: A = V^T from transposed ldmatrix
+//            tiles (16 dims x 16 keys), B = P split as hi + lo (with at most
+//            four query heads per KV head the lo parts fill the idle columns
+//            4..7; otherwise a second product).
+// The softmax runs in the score fragment (each lane holds two keys of one
+// head) with lazily raised maxima.
 //
-// Rotation accuracy.  Delta(j) reaches ~1e5, so its angle is reduced in
-// double precision once per CTA (first block); later blocks step the base
-// by R_{-n} with 0 <= n <= 64 from a per-CTA table, and within a block
-// key j0 + t uses base(j0) * R_{-n(t)}.  The R_{-n} table is built from
-// R_{-b} and R_{-8a} with the frequency split in two floats so that
-// n * omega_hi is exact.
+// Correction rotations.  Keys are grouped in 64-key table blocks from the
+// slice start j0 = js + 64 b.  Within a block, key j0 + t needs
+// R_{Delta(j0+t)} = R_{Delta(j0)} R_{-n(t)}, n(t) = t - (f(j0+t) - f(j0)) in
+// [0, 63], and R_{-n} = R_{-8a} R_{-c} (n = 8a + c) comes from two small
+// per-CTA tables.  The block base R_{Delta(j0)} is reduced in double
+// precision once per CTA and then stepped block to block by R_{-n64},
+// n64 = 64 - (f(j0+64) - f(j0)).  Each thread owns one frequency pair of the
+// table and keeps that pair's base in registers.  The tables of two blocks
+// are double-buffered: while the warps stream block b they build block b+1's
+// table, a few entries per step, so one CTA barrier per block suffices.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -56,29 +64,26 @@
 namespace jl {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kBlockKeys = 64;  // keys per rotation-table block
-constexpr int kStep = 8;        // keys per warp step
+constexpr int kStep = 16;       // keys per warp step
 constexpr int kStages = 2;      // per-warp ring depth
-// Warps sharing a KV head (alternate steps): two while the query fragments
-// of a head group fit the 128-register budget of a 512-thread CTA, one for
-// eight query heads per KV head.
-__host__ __device__ constexpr int warps_per_head(int gq) { return gq <= 4 ? 2 : 1; }
+constexpr int kMaxHeadsPerCta = 8;
+constexpr int kMaxWarps = 8;
 constexpr int kMaxSplits = 512;
-constexpr int kMinBlocksPerSplit = 8;  // batched decode: blocks per slice when the batch fills the SMs
-constexpr int kStageBytes = kStep * 2 * kD * 2;  // K and V rows of one step
-constexpr float kRescaleThreshold = 8.0f;        // log2 units
-constexpr int kTabStride = 36;  // float4 per key row of the rotation table (32 + 4 padding)
+constexpr int kMinStepsPerSplit = 32;  // batched decode: steps per slice when the batch fills the SMs
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSmallRows = 17;             // R_{-c} (c < 8), then R_{-8a} (a <= 8)
 
 struct DecodeKParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kc;
   const __nv_bfloat16* vc;
-  float* part_o;   // [nsplit, B, Hq, 128]
-  float* part_ml;  // [nsplit, B, Hq, 2]
+  float* part_o;   // [slices, B, Hq, D]
+  float* part_ml;  // [slices, B, Hq, 2]
   int* status;     // device status word
   const int* seqlens;  // per-sequence lengths [B] (device) or nullptr: every sequence has length L
-  int B, L, Lcap, Hq, Hkv, w0, G, wp, keys_per_split;
+  int B, L, Lcap, Hq, Hkv, gq, hpc, wph, w0, G, wp;
+  int steps_base, steps_extra;  // slice s holds steps_base + (s < steps_extra) 16-key steps
   float scale_log2;
   RopeFreqs freqs;
 };
@@ -113,12 +118,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
 // Two floats to bf16x2 (x in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -134,31 +133,71 @@ __device__ __forceinline__ void split_bf16(float2 v, uint32_t& hi, uint32_t& lo)
   const float2 r = __ffma2_rn(unpack_bf16(hi), make_float2(-1.f, -1.f), v);
   lo = pack_bf16(r.x, r.y);
 }
+// Rotates the bf16 pairs (x_i, x_i+1) and (y_i, y_i+1) (rotate-half
+// partners) by the table entry t = {cos_i, cos_i+1, sin_i, sin_i+1}:
+// (x, y) -> (x c - y s, y c + x s), split into bf16 hi and lo words.
+__device__ __forceinline__ void rotate_split(uint32_t xw, uint32_t yw, const float4 t, uint32_t& xh, uint32_t& xl,
+                                             uint32_t& yh, uint32_t& yl) {
+  const float2 x = unpack_bf16(xw), y = unpack_bf16(yw);
+  const float2 c = make_float2(t.x, t.y), s = make_float2(t.z, t.w);
+  split_bf16(__ffma2_rn(y, neg2(s), __fmul2_rn(x, c)), xh, xl);
+  split_bf16(__ffma2_rn(x, s, __fmul2_rn(y, c)), yh, yl);
+}
 
-template <int GQ>
-__global__ void __launch_bounds__(warps_per_head(GQ) * 256, 1)
+// Rotations of two frequencies at once: (c, s) = (cos, sin) of frequencies
+// (i, i + 1), turned further by the rotation in t = {cos_i, cos_i+1, sin_i,
+// sin_i+1} (angles add).
+__device__ __forceinline__ void turn2(float2& c, float2& s, const float4 t) {
+  const float2 tc = make_float2(t.x, t.y), ts = make_float2(t.z, t.w);
+  const float2 nc = __ffma2_rn(s, neg2(ts), __fmul2_rn(c, tc));
+  const float2 ns = __ffma2_rn(c, ts, __fmul2_rn(s, tc));
+  c = nc;
+  s = ns;
+}
+
+// floor(a / G) for 0 <= a < G + 64 (a < 128 when G < 64): the quotient is 0
+// or 1 once G >= 64; below that (a + 0.5) / G in float is far enough from an
+// integer that the float quotient floors exactly.
+__device__ __forceinline__ int div_small(int a, int G, float invG) {
+  if (G >= 64) return a >= G ? 1 : 0;
+  return static_cast<int>(__fmul_rn(static_cast<float>(a) + 0.5f, invG));
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
 decode_partial_kernel(DecodeKParams p) {
-  constexpr int kWarpsPerHead = warps_per_head(GQ);
   constexpr int kNT = (GQ + 3) / 4;                // score n-tiles: 4 heads x {hi, lo} each
-  constexpr int kBlockSteps = kBlockKeys / kStep;  // global steps per table block (8)
+  constexpr int kHalf = D / 2;
+  constexpr int kQuads = D / 4;                    // table entries (frequency pairs) per key
+  constexpr int kRowChunks = D / 8;                // 16-byte chunks per cache row
+  constexpr int kRowsPerCopy = 32 / kRowChunks;    // rows one warp-wide copy covers
+  constexpr int kCopies = kStep / kRowsPerCopy;    // copies per step and matrix
+  constexpr int kStageBytes = kStep * 2 * D * 2;   // K and V rows of one step
+  constexpr int kVOff = kStep * D * 2;             // V rows within a stage
+  constexpr int kSC = D / 32;                      // score chunks of 16 dims (+ rotate-half partner)
+  constexpr int kMT = D / 16;                      // O^T m-tiles of 16 dims
+  constexpr int kBlockSteps = kBlockKeys / kStep;  // global steps per table block (4)
+  constexpr int kTabEntries = kBlockKeys * kQuads;
   // P V columns: with GQ <= 4, column n holds head n & 3, its P hi part for
   // n < 4 and its lo part for n >= 4; with GQ = 8 column n is head n.
   constexpr bool kLoCols = GQ <= 4;
   auto hcol = [](int n) { return kLoCols ? (n & 3) : n; };
+  const int gq = p.gq;    // query heads per KV head (<= GQ)
+  const int wph = p.wph;  // warps per KV head (1, 2 or 4), alternate steps
+  const int block_local = kBlockSteps / wph;  // steps per warp per table block
+
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // Region A: the rotated queries during set-up, then the rotation table of
-  // the current 64-key block: [key][kTabStride] float4 {cos_i, cos_i+1,
-  // sin_i, sin_i+1} for the frequency pair (i, i+1), i = 2 * index.
-  float* s_qa = reinterpret_cast<float*>(smem_raw);  // [Hq][128], pre-scaled
-  float* s_qr = s_qa + p.Hq * kD;                    // [Hq][128]
-  const float4* s_tab = reinterpret_cast<const float4*>(smem_raw);
-  float4* s_tab_w = reinterpret_cast<float4*>(smem_raw);
-  const int region_a = max(2 * p.Hq * kD * 4, kBlockKeys * kTabStride * 16);
-  float2* s_lo = reinterpret_cast<float2*>(smem_raw + region_a);  // [8][64]: R_{-b}
-  float2* s_hi = s_lo + 8 * 64;                                   // [9][64]: R_{-8a}
-  float2* s_base = s_hi + 9 * 64;                                 // [64]
-  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_base + 64);
-  __shared__ float2 s_qcs[2][64];
+  // Two rotation tables [64 keys][kQuads] float4 {cos_i, cos_i+1, sin_i,
+  // sin_i+1}, entry (t, pp) at column pp ^ 4 (t & 1) so that the fragment
+  // reads are free of bank conflicts; then the small tables, the first
+  // block's base, the query rotations, and the per-warp rings.  The raw
+  // query rows are staged in the second table buffer during the set-up.
+  float4* s_tab = reinterpret_cast<float4*>(smem_raw);
+  float4* s_small = s_tab + 2 * kTabEntries;                                    // [17][kQuads]
+  float2* s_base0 = reinterpret_cast<float2*>(s_small + kSmallRows * kQuads);  // [kHalf]
+  float2* s_qcs = s_base0 + kHalf;                                              // [2][kHalf]
+  unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_qcs + 2 * kHalf);
+  const __nv_bfloat16* s_q = reinterpret_cast<const __nv_bfloat16*>(s_tab + kTabEntries);
 
   // Let the merge kernel (a programmatic dependent) launch early; it waits
   // for this grid's completion before reading the partials.
@@ -174,131 +213,190 @@ decode_partial_kernel(DecodeKParams p) {
   if (p.seqlens != nullptr) {
     L = p.seqlens[b];
     if (L < 1 || L > p.Lcap) {
-      if (threadIdx.x == 0 && split == 0) atomicCAS(p.status, 0, 30);
+      if (threadIdx.x == 0 && split == 0 && blockIdx.z == 0) atomicCAS(p.status, 0, 30);
       L = min(max(L, 1), p.Lcap);
     }
     G = static_cast<int>(group_size(L, p.wp));
   }
-  const int js = split * p.keys_per_split;
-  const int je = max(js, min(L, js + p.keys_per_split));  // empty slice past the sequence end
+  const long long step0 = static_cast<long long>(split) * p.steps_base + min(split, p.steps_extra);
+  const long long nstep_slice = p.steps_base + (split < p.steps_extra ? 1 : 0);
+  const int js = static_cast<int>(min(static_cast<long long>(L), kStep * step0));
+  const int je = static_cast<int>(min(static_cast<long long>(L), kStep * (step0 + nstep_slice)));
   const int qpos = L - 1;
   const bool bifocal = G > 1;
   const int first_local = qpos - p.w0;  // keys j >= first_local are local
 
-  // kWarpsPerHead warps per KV head: warp `par` of a head takes the global
-  // steps it = kWarpsPerHead * u + par.
-  const int hk = warp % p.Hkv, par = warp / p.Hkv;
-  const long long row_stride = static_cast<long long>(p.Hkv) * kD;
-  const __nv_bfloat16* kbase = p.kc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
-  const __nv_bfloat16* vbase = p.vc + (static_cast<long long>(b) * p.Lcap * p.Hkv + hk) * kD;
+  // Warp `par` of KV head hkl takes the global steps it = wph * u + par.
+  // KV heads past Hkv (last head group) stream nothing but keep the CTA's
+  // barrier count.
+  const int hkl = warp % p.hpc, par = warp / p.hpc;
+  const int hk0 = blockIdx.z * p.hpc;
+  const int hk = hk0 + hkl;
+  const bool head_ok = hk < p.Hkv;
+  const long long row_stride = static_cast<long long>(p.Hkv) * D;
+  const long long cache_off = (static_cast<long long>(b) * p.Lcap * p.Hkv + (head_ok ? hk : 0)) * D;
+  const __nv_bfloat16* kbase = p.kc + cache_off;
+  const __nv_bfloat16* vbase = p.vc + cache_off;
   unsigned char* my_ring = s_ring + warp * kStages * kStageBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(my_ring));
-  const int nsteps = (je - js + kStep - 1) / kStep;
-  const int nlocal = (nsteps + kWarpsPerHead - 1) / kWarpsPerHead;  // local steps (warp 0 of a head)
+  const int nsteps_all = (je - js + kStep - 1) / kStep;
+  const int nsteps = head_ok ? nsteps_all : 0;
+  const int nlocal = (nsteps_all + wph - 1) / wph;  // same for every warp
 
-  // Stage layout: K rows of the step's 8 keys (256 B each), then V rows.
+  // The CTA's raw query rows (query heads hk0 * gq ..), one cp.async group.
+  {
+    const int nh = min(p.hpc, p.Hkv - hk0) * gq;
+    const __nv_bfloat16* qsrc = p.q + (static_cast<long long>(b) * p.Hq + hk0 * gq) * D;
+    const uint32_t qdst = static_cast<uint32_t>(__cvta_generic_to_shared(s_q));
+    for (int c = tid; c < nh * (D / 8); c += nthr) cp_async16(qdst + 16 * c, qsrc + 8 * c, 16);
+    cp_async_commit();
+  }
+
+  // Stage layout: K rows of the step's 16 keys (2D bytes each), then V rows.
   // 16-byte chunk c of key row r sits at chunk c ^ (r & 7) of its row, so
   // that the eight rows of an 8x8 ldmatrix tile fall in eight bank groups.
-  // Lane roles of the copies: chunk c = lane & 15 of key 2 i + (lane >> 4).
-  const long long lane_src = static_cast<long long>(lane >> 4) * row_stride + (lane & 15) * 8;
-  // Destination of copy i (key 2 i + (lane >> 4), swizzled chunk), relative to the stage.
-  uint32_t lane_dst[4];
+  const int crow = lane / kRowChunks, cchunk = lane % kRowChunks;
+  const long long lane_src = crow * row_stride + cchunk * 8;
+  const long long copy_stride = kRowsPerCopy * row_stride;
+  uint32_t lane_dst[kCopies];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int key = 2 * i + (lane >> 4);
-    lane_dst[i] = static_cast<uint32_t>((key * 16 + ((lane & 15) ^ key)) * 16);
+  for (int i = 0; i < kCopies; ++i) {
+    const int key = kRowsPerCopy * i + crow;
+    lane_dst[i] = static_cast<uint32_t>((key * kRowChunks + (cchunk ^ (key & 7))) * 16);
   }
   auto issue_step = [&](int u) {
-    const int it = kWarpsPerHead * u + par;
+    const int it = wph * u + par;
     if (it < nsteps) {
       const int jstep = js + it * kStep;
-      const uint32_t st = ring + static_cast<uint32_t>((u % kStages) * kStageBytes);
+      const uint32_t st = ring + static_cast<uint32_t>((u & (kStages - 1)) * kStageBytes);
+      const __nv_bfloat16* kp = kbase + lane_src + static_cast<long long>(jstep) * row_stride;
+      const __nv_bfloat16* vp = vbase + lane_src + static_cast<long long>(jstep) * row_stride;
       if (jstep + kStep <= je) {  // full step: no bounds checks
-        const __nv_bfloat16* kp = kbase + lane_src + static_cast<long long>(jstep) * row_stride;
-        const __nv_bfloat16* vp = vbase + lane_src + static_cast<long long>(jstep) * row_stride;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          cp_async16(st + lane_dst[i], kp + 2 * i * row_stride, 16);
-          cp_async16(st + 2048 + lane_dst[i], vp + 2 * i * row_stride, 16);
+        for (int i = 0; i < kCopies; ++i) {
+          cp_async16(st + lane_dst[i], kp + i * copy_stride, 16);
+          cp_async16(st + kVOff + lane_dst[i], vp + i * copy_stride, 16);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const bool ok = jstep + 2 * i + (lane >> 4) < je;
-          const long long off = ok ? lane_src + static_cast<long long>(jstep + 2 * i) * row_stride : 0;
-          cp_async16(st + lane_dst[i], kbase + off, ok ? 16 : 0);
-          cp_async16(st + 2048 + lane_dst[i], vbase + off, ok ? 16 : 0);
+        for (int i = 0; i < kCopies; ++i) {
+          const bool ok = jstep + kRowsPerCopy * i + crow < je;
+          cp_async16(st + lane_dst[i], ok ? kp + i * copy_stride : kbase, ok ? 16 : 0);
+          cp_async16(st + kVOff + lane_dst[i], ok ? vp + i * copy_stride : vbase, ok ? 16 : 0);
         }
       }
     }
     cp_async_commit();
   };
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) issue_step(s);
+  for (int s = 0; s < kStages; ++s) issue_step(s);
 
-  // Query rotations R_{L-1} and R_{f(L-1)}, and the small rotation tables.
-  for (int i = tid; i < 64; i += nthr) {
-    s_qcs[0][i] = rope_cos_sin(qpos, p.freqs.w[i]);
-    s_qcs[1][i] = rope_cos_sin(alias(qpos, G), p.freqs.w[i]);
+  // ---- Set-up, while the query rows and the first two steps are in flight ----
+  // Query rotations R_{L-1} and R_{f(L-1)}, the first block's base
+  // R_{Delta(js)} (angles reduced in double), and the small tables R_{-c}
+  // (c < 8) and R_{-8a} (a <= 8) with omega = hi + lo, hi holding 17
+  // significant bits so that n * hi is exact in float for n <= 64.
+  const bool any_remote = bifocal && js < first_local && js < je;
+  for (int i = tid; i < kHalf * (any_remote ? 3 : 2); i += nthr) {
+    const int which = i / kHalf, f = i % kHalf;
+    const long long pos = which == 0 ? qpos : which == 1 ? alias(qpos, G) : alias_offset(js, G);
+    const float2 cs = rope_cos_sin(pos, p.freqs.w[f]);
+    if (which < 2)
+      s_qcs[which * kHalf + f] = cs;
+    else
+      s_base0[f] = cs;
   }
-  const bool any_remote = bifocal && js < first_local;
   if (any_remote) {
-    // R_{-b} (b < 8) and R_{-8a} (a <= 8) with omega = hi + lo, hi holding
-    // 17 significant bits so that n * hi is exact in float for n <= 64.
-    for (int idx = tid; idx < 17 * 64; idx += nthr) {
-      const int r = idx / 64, i = idx % 64;
+    for (int idx = tid; idx < kSmallRows * kQuads; idx += nthr) {
+      const int r = idx / kQuads, pp = idx % kQuads;
       const int n = r < 8 ? r : 8 * (r - 8);
-      const double w = p.freqs.w[i];
-      const float whi = __uint_as_float(__float_as_uint(static_cast<float>(w)) & 0xffffff80u);
-      const float wlo = static_cast<float>(w - static_cast<double>(whi));
-      float sn, cn;
-      sincosf(static_cast<float>(n) * whi, &sn, &cn);
-      const float e = static_cast<float>(n) * wlo;  // |e| < 1e-3
-      const float2 rr = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
-      (r < 8 ? s_lo : s_hi)[(r < 8 ? r : r - 8) * 64 + i] = make_float2(rr.x, -rr.y);  // R_{-n}
+      float2 cs[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const double w = p.freqs.w[2 * pp + k];
+        const float whi = __uint_as_float(__float_as_uint(static_cast<float>(w)) & 0xffffff80u);
+        const float wlo = static_cast<float>(w - static_cast<double>(whi));
+        float sn, cn;
+        sincosf(static_cast<float>(n) * whi, &sn, &cn);
+        const float e = static_cast<float>(n) * wlo;  // |e| < 1e-3
+        cs[k] = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
+      }
+      s_small[idx] = make_float4(cs[0].x, cs[1].x, -cs[0].y, -cs[1].y);  // R_{-n}
     }
-    for (int i = tid; i < 64; i += nthr) s_base[i] = rope_cos_sin(alias_offset(js, G), p.freqs.w[i]);
   }
+  cp_async_wait<kStages>();  // the query rows (the oldest group) have landed
   __syncthreads();
-  const __nv_bfloat16* qin = p.q + static_cast<long long>(b) * p.Hq * kD;
-  for (int idx = tid; idx < p.Hq * 64; idx += nthr) {
-    const int h = idx / 64, i = idx % 64;
-    const float x = __bfloat162float(qin[h * kD + i]);
-    const float y = __bfloat162float(qin[h * kD + 64 + i]);
-    const float2 ra = rotate_pair(x, y, s_qcs[0][i]);
-    const float2 rr = rotate_pair(x, y, s_qcs[1][i]);
-    s_qa[h * kD + i] = ra.x * p.scale_log2;
-    s_qa[h * kD + 64 + i] = ra.y * p.scale_log2;
-    s_qr[h * kD + i] = rr.x * p.scale_log2;
-    s_qr[h * kD + 64 + i] = rr.y * p.scale_log2;
-  }
-  __syncthreads();
+
   // Query operands of the score MMA (B, 16 dims x 8 columns per chunk):
   // column n of n-tile nt is head 4 nt + n / 2, hi part (n even) or lo part
   // (n odd) of the pre-scaled rotated query; variant 0 absolute, 1 aliased.
-  uint32_t qf[2][kNT][8][2];
+  // Chunk c < kSC holds the first-half dims 16 c + 8 e + 2 t4 (+1) and chunk
+  // c + kSC their rotate-half partners, so each lane rotates its own pairs.
+  uint32_t qf[2][kNT][kMT][2];
 #pragma unroll
-  for (int v = 0; v < 2; ++v)
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int hl = 4 * nt + (g >> 1);
+    const bool valid = head_ok && hl < gq;
+    const __nv_bfloat16* qrow = s_q + (valid ? hkl * gq + hl : 0) * D;
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const int hl = 4 * nt + (g >> 1);
-      const float* qrow = (v ? s_qr : s_qa) + (hk * GQ + (hl < GQ ? hl : 0)) * kD;
+    for (int c = 0; c < kSC; ++c)
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
+      for (int e = 0; e < 2; ++e) {
+        const int i = 16 * c + 8 * e + 2 * t4;
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(qrow + i));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(qrow + kHalf + i));
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int v = 0; v < 2; ++v) {
+          const float2 c0 = s_qcs[v * kHalf + i], c1 = s_qcs[v * kHalf + i + 1];
+          const float2 cc = make_float2(c0.x, c1.x), ss = make_float2(c0.y, c1.y);
+          const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+          const float2 rx = __fmul2_rn(__ffma2_rn(y, neg2(ss), __fmul2_rn(x, cc)), sc);
+          const float2 ry = __fmul2_rn(__ffma2_rn(x, ss, __fmul2_rn(y, cc)), sc);
           uint32_t hi, lo;
-          split_bf16(*reinterpret_cast<const float2*>(qrow + 16 * c + 8 * e + 2 * t4), hi, lo);
-          qf[v][nt][c][e] = hl < GQ ? ((g & 1) ? lo : hi) : 0u;
+          split_bf16(rx, hi, lo);
+          qf[v][nt][c][e] = valid ? ((g & 1) ? lo : hi) : 0u;
+          split_bf16(ry, hi, lo);
+          qf[v][nt][c + kSC][e] = valid ? ((g & 1) ? lo : hi) : 0u;
         }
+      }
+  }
+
+  // Rotation-table state of this thread: frequency pair pp (fixed, since
+  // nthr is a multiple of 32 >= kQuads), the base of the block being built,
+  // and j0 mod G of that block.
+  const int pp = tid % kQuads;
+  const int entries_per_thread = (kTabEntries + nthr - 1) / nthr;
+  const int per_step = (entries_per_thread + block_local - 1) / block_local;
+  const float invG = 1.0f / static_cast<float>(G);
+  float2 bc = make_float2(1.f, 1.f), bs = make_float2(0.f, 0.f);
+  int r0 = 0;
+  auto build_entries = [&](int buf, int k0, int k1) {
+    float4* tab = s_tab + buf * kTabEntries;
+    for (int k = k0; k < k1; ++k) {
+      const int e = tid + nthr * k;
+      if (e >= kTabEntries) break;
+      const int t = e / kQuads;
+      const int n = t - div_small(r0 + t, G, invG);  // 0..63
+      float2 c = bc, s = bs;
+      turn2(c, s, s_small[(8 + (n >> 3)) * kQuads + pp]);
+      turn2(c, s, s_small[(n & 7) * kQuads + pp]);
+      tab[t * kQuads + (pp ^ ((t & 1) << 2))] = make_float4(c.x, c.y, s.x, s.y);
     }
-  // (The first table build below starts with a barrier, after which the
-  // table may overwrite the rotated queries.)
+  };
+  if (any_remote) {
+    const float2 b0 = s_base0[2 * pp], b1 = s_base0[2 * pp + 1];
+    bc = make_float2(b0.x, b1.x);
+    bs = make_float2(b0.y, b1.y);
+    r0 = js % G;
+  }
+  __syncthreads();  // query rows read; their buffer becomes table 1
+  if (any_remote) build_entries(0, 0, entries_per_thread);
+  __syncthreads();  // table of block 0 complete
 
   // O^T accumulators: m-tile mt holds dims 16 mt + g (+8) of heads 2 t4, 2 t4 + 1.
-  float o[8][4];
+  float o[kMT][4];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+  for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
   // Softmax state of head 4 nt + t4 (the same in the 8 lanes of a column).
@@ -308,205 +406,202 @@ decode_partial_kernel(DecodeKParams p) {
     m_run[nt] = -INFINITY;
     l_run[nt] = 0.f;
   }
-  // ldmatrix lane roles: lanes 8 mi .. 8 mi + 7 address rows 0..7 of tile mi.
-  const int lm = lane >> 3, lr = lane & 7;
+  // ldmatrix lane roles.  Scores (A, 16 keys x 16 dims): lane l addresses key
+  // (l & 7) + 8 ((l >> 3) & 1) at chunk 2 c + (l >> 4).  P V (A = V^T, 16
+  // dims x 16 keys, transposed): key (l & 7) + 8 (l >> 4) at chunk 2 mt +
+  // ((l >> 3) & 1).  Offsets relative to the stage, per chunk index.
+  const int ka = (lane & 7) + 8 * ((lane >> 3) & 1), kb = (lane & 7) + 8 * (lane >> 4);
+  const uint32_t a_row = static_cast<uint32_t>(ka * 2 * D), b_row = static_cast<uint32_t>(kVOff + kb * 2 * D);
+  const int a_sw = ka & 7, b_sw = kb & 7, a_hi = lane >> 4, b_hi = (lane >> 3) & 1;
+  const int sw = (g & 1) << 2;  // table column swizzle of this lane's keys (g and g + 8)
 
-  constexpr int kBlockLocal = kBlockSteps / kWarpsPerHead;  // local steps per table block
   for (int u = 0; u < nlocal; ++u) {
-    const int it = kWarpsPerHead * u + par;
-    const int blk = u / kBlockLocal;
+    const int it = wph * u + par;
+    const int blk = u / block_local, ub = u - blk * block_local;
     const int j0 = js + blk * kBlockKeys;  // table block base
-    if ((u % kBlockLocal) == 0) {
-      __syncthreads();  // previous table (or the rotated queries) no longer read
-      if (bifocal && j0 < first_local) {
-        if (blk > 0) {
-          const int n = alias_offset(j0 - kBlockKeys, G) - alias_offset(j0, G);  // 0..64
-          for (int i = tid; i < 64; i += nthr)
-            s_base[i] = compose(compose(s_base[i], s_hi[(n >> 3) * 64 + i]), s_lo[(n & 7) * 64 + i]);
-          __syncthreads();
-        }
-        const int fj0 = alias(j0, G);
-        for (int idx = tid; idx < kBlockKeys * 32; idx += nthr) {
-          const int t = idx >> 5, pp = idx & 31, i0 = 2 * pp;
-          const int n = t - (alias(j0 + t, G) - fj0);  // 0..63
-          const float2 c0 =
-              compose(compose(s_base[i0], s_hi[(n >> 3) * 64 + i0]), s_lo[(n & 7) * 64 + i0]);
-          const float2 c1 = compose(compose(s_base[i0 + 1], s_hi[(n >> 3) * 64 + i0 + 1]),
-                                    s_lo[(n & 7) * 64 + i0 + 1]);
-          s_tab_w[t * kTabStride + pp] = make_float4(c0.x, c1.x, c0.y, c1.y);
-        }
+    // Block blk's table was built during block blk - 1 (or the set-up);
+    // after this barrier nobody reads block blk - 1's buffer any more.
+    if (ub == 0 && blk > 0) __syncthreads();
+    // Part of the next block's table (remote keys form a prefix of [0, L)).
+    if (bifocal && j0 + kBlockKeys < first_local && j0 + kBlockKeys < je) {
+      if (ub == 0) {  // base and residue of block blk + 1
+        const int q64 = div_small(r0 + kBlockKeys, G, invG);
+        const int n = kBlockKeys - q64;  // 0..64
+        turn2(bc, bs, s_small[(8 + (n >> 3)) * kQuads + pp]);
+        turn2(bc, bs, s_small[(n & 7) * kQuads + pp]);
+        r0 += kBlockKeys - q64 * G;
       }
-      __syncthreads();
+      build_entries((blk + 1) & 1, ub * per_step, min((ub + 1) * per_step, entries_per_thread));
     }
-    issue_step(u + kStages - 1);
     cp_async_wait<kStages - 1>();
     __syncwarp();
-    if (it >= nsteps) continue;
+    if (it < nsteps) {
+      const int jstep = js + it * kStep;
+      const uint32_t st = ring + static_cast<uint32_t>((u & (kStages - 1)) * kStageBytes);
+      const bool all_local = !bifocal || jstep >= first_local;
+      const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
 
-    const int jstep = js + it * kStep;
-    const uint32_t st = ring + static_cast<uint32_t>((u % kStages) * kStageBytes);
-    const bool all_local = !bifocal || jstep >= first_local;
-    const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
-
-    // Scores z[nt] of (key jstep + g, head 4 nt + t4) in log2 units.
-    float z[kNT];
+      // Scores z[nt][r] of (key jstep + g + 8 r, head 4 nt + t4), log2 units.
+      float z[kNT][2];
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) z[nt] = 0.f;
-    if (!all_local) {
-      // Aliased scores.  A = the step's 8 keys corrected by R_{f(j) - j},
-      // rows 0..7 their bf16 hi parts, rows 8..15 the lo parts; chunk c
-      // (dims 16 c ..) and chunk c + 4 (the rotate-half partners) together.
-      float acc0[kNT][4], acc1[kNT][4];
+      for (int nt = 0; nt < kNT; ++nt) z[nt][0] = z[nt][1] = 0.f;
+      if (!all_local) {
+        // Aliased scores.  A = the step's 16 keys corrected by R_{f(j) - j},
+        // once with their bf16 hi parts and once with the lo parts; chunk c
+        // (dims 16 c ..) and chunk c + kSC (the rotate-half partners).
+        float acc[kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
+        for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc0[nt][e] = acc1[nt][e] = 0.f;
-      const float4* tab = s_tab + (jstep - j0 + g) * kTabStride + t4;
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        const float4* tab0 = s_tab + (blk & 1) * kTabEntries + (jstep - j0 + g) * kQuads;
+        const float4* tab1 = tab0 + 8 * kQuads;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r0, r1, r2, r3;
-        const int ch = 2 * c + (lm & 1) + 8 * (lm >> 1);
-        ldsm_x4(st + static_cast<uint32_t>(lr * 256 + ((ch ^ lr) << 4)), r0, r1, r2, r3);
-        const float4 cs0 = tab[8 * c], cs1 = tab[8 * c + 4];
-        const float2 x0 = unpack_bf16(r0), x1 = unpack_bf16(r1), y0 = unpack_bf16(r2), y1 = unpack_bf16(r3);
-        const float2 c0 = make_float2(cs0.x, cs0.y), s0 = make_float2(cs0.z, cs0.w);
-        const float2 c1 = make_float2(cs1.x, cs1.y), s1 = make_float2(cs1.z, cs1.w);
-        // (x, y) -> (x c - y s, y c + x s)
-        const float2 nx0 = __ffma2_rn(y0, neg2(s0), __fmul2_rn(x0, c0));
-        const float2 ny0 = __ffma2_rn(x0, s0, __fmul2_rn(y0, c0));
-        const float2 nx1 = __ffma2_rn(y1, neg2(s1), __fmul2_rn(x1, c1));
-        const float2 ny1 = __ffma2_rn(x1, s1, __fmul2_rn(y1, c1));
-        uint32_t x0h, x0l, x1h, x1l, y0h, y0l, y1h, y1l;
-        split_bf16(nx0, x0h, x0l);
-        split_bf16(nx1, x1h, x1l);
-        split_bf16(ny0, y0h, y0l);
-        split_bf16(ny1, y1h, y1l);
+        for (int c = 0; c < kSC; ++c) {
+          uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+          ldsm_x4(st + a_row + static_cast<uint32_t>(((2 * c + a_hi) ^ a_sw) << 4), x0, x1, x2, x3);
+          ldsm_x4(st + a_row + static_cast<uint32_t>(((D / 16 + 2 * c + a_hi) ^ a_sw) << 4), y0, y1, y2, y3);
+          // x0/y0: key g, dims 16 c + 2 t4 (+1); x1/y1: key g + 8, same dims;
+          // x2/y2: key g, dims 16 c + 8 + 2 t4; x3/y3: key g + 8, those dims.
+          uint32_t h[8], l[8];
+          rotate_split(x0, y0, tab0[(8 * c + t4) ^ sw], h[0], l[0], h[4], l[4]);
+          rotate_split(x1, y1, tab1[(8 * c + t4) ^ sw], h[1], l[1], h[5], l[5]);
+          rotate_split(x2, y2, tab0[(8 * c + 4 + t4) ^ sw], h[2], l[2], h[6], l[6]);
+          rotate_split(x3, y3, tab1[(8 * c + 4 + t4) ^ sw], h[3], l[3], h[7], l[7]);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma16816(acc[nt], h[0], h[1], h[2], h[3], qf[1][nt][c][0], qf[1][nt][c][1]);
+            mma16816(acc[nt], l[0], l[1], l[2], l[3], qf[1][nt][c][0], qf[1][nt][c][1]);
+            mma16816(acc[nt], h[4], h[5], h[6], h[7], qf[1][nt][c + kSC][0], qf[1][nt][c + kSC][1]);
+            mma16816(acc[nt], l[4], l[5], l[6], l[7], qf[1][nt][c + kSC][0], qf[1][nt][c + kSC][1]);
+          }
+        }
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          mma16816(acc0[nt], x0h, x0l, x1h, x1l, qf[1][nt][c][0], qf[1][nt][c][1]);
-          mma16816(acc1[nt], y0h, y0l, y1h, y1l, qf[1][nt][c + 4][0], qf[1][nt][c + 4][1]);
+          z[nt][0] = acc[nt][0] + acc[nt][1];
+          z[nt][1] = acc[nt][2] + acc[nt][3];
         }
       }
+      if (!all_remote) {
+        // Absolute scores: the cached keys as stored (exact in bf16).
+        float acc[kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-        z[nt] = ((acc0[nt][0] + acc0[nt][1]) + (acc0[nt][2] + acc0[nt][3])) +
-                ((acc1[nt][0] + acc1[nt][1]) + (acc1[nt][2] + acc1[nt][3]));
-    }
-    if (!all_remote) {
-      // Absolute scores: the cached keys as stored (exact in bf16, lo rows 0).
-      float acc0[kNT][4], acc1[kNT][4];
+        for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc0[nt][e] = acc1[nt][e] = 0.f;
+        for (int c = 0; c < kSC; ++c) {
+          uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+          ldsm_x4(st + a_row + static_cast<uint32_t>(((2 * c + a_hi) ^ a_sw) << 4), x0, x1, x2, x3);
+          ldsm_x4(st + a_row + static_cast<uint32_t>(((D / 16 + 2 * c + a_hi) ^ a_sw) << 4), y0, y1, y2, y3);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r0, r1, r2, r3;
-        const int ch = 2 * c + (lm & 1) + 8 * (lm >> 1);
-        ldsm_x4(st + static_cast<uint32_t>(lr * 256 + ((ch ^ lr) << 4)), r0, r1, r2, r3);
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma16816(acc[nt], x0, x1, x2, x3, qf[0][nt][c][0], qf[0][nt][c][1]);
+            mma16816(acc[nt], y0, y1, y2, y3, qf[0][nt][c + kSC][0], qf[0][nt][c + kSC][1]);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const bool local = all_local || is_local(qpos, jstep + g + 8 * r, p.w0);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt)
+            if (local) z[nt][r] = acc[nt][2 * r] + acc[nt][2 * r + 1];
+        }
+      }
+
+      // Online softmax per head (column); the max used for the exponentials
+      // is raised only when it grows by more than kRescaleThreshold.
+      bool any_rescale = false;
+      float pr[kNT][2], al[kNT];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        const bool hv = 4 * nt + t4 < gq;
+        const float z0 = hv && jstep + g < je ? z[nt][0] : -INFINITY;
+        const float z1 = hv && jstep + g + 8 < je ? z[nt][1] : -INFINITY;
+        float bm = fmaxf(z0, z1);
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        float alpha = 1.f;
+        if (bm > m_run[nt] + kRescaleThreshold) {
+          alpha = exp2f(m_run[nt] - bm);
+          m_run[nt] = bm;
+        }
+        const float mexp = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
+        pr[nt][0] = exp2f(z0 - mexp);
+        pr[nt][1] = exp2f(z1 - mexp);
+        l_run[nt] = l_run[nt] * alpha + (pr[nt][0] + pr[nt][1]);
+        al[nt] = alpha;
+        any_rescale |= alpha != 1.f;
+      }
+      any_rescale = __any_sync(0xffffffffu, any_rescale);
+      if (any_rescale) {
+        // Column n of O^T belongs to head hcol(n); its alpha sits in lane
+        // hcol & 3 of n-tile hcol >> 2.
+        float ae = 1.f, ao = 1.f;
+        const int he = hcol(2 * t4), ho = hcol(2 * t4 + 1);
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          mma16816(acc0[nt], r0, 0u, r1, 0u, qf[0][nt][c][0], qf[0][nt][c][1]);
-          mma16816(acc1[nt], r2, 0u, r3, 0u, qf[0][nt][c + 4][0], qf[0][nt][c + 4][1]);
+          const float x = __shfl_sync(0xffffffffu, al[nt], he & 3);
+          const float y = __shfl_sync(0xffffffffu, al[nt], ho & 3);
+          if ((he >> 2) == nt) ae = x;
+          if ((ho >> 2) == nt) ao = y;
+        }
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt) {
+          o[mt][0] *= ae;
+          o[mt][1] *= ao;
+          o[mt][2] *= ae;
+          o[mt][3] *= ao;
         }
       }
-      const bool local = !bifocal || jstep + g >= first_local;
+      // P^T operand (B, 16 keys x 8 columns): keys 2 t4, 2 t4 + 1 (b0) and
+      // 2 t4 + 8, 2 t4 + 9 (b1) of column g, i.e. of head hcol(g); key k < 8
+      // of head hh sits in lane 4 k + (hh & 3), key k + 8 in the same lane's
+      // second slot.  P is split as hi + lo in bf16: with GQ <= 4 the lo
+      // parts fill columns 4..7, otherwise they go through a second product.
+      uint32_t pb_hi[2], pb_lo[2];
+      {
+        const int hh = hcol(g);
+        const int src = 8 * t4 + (hh & 3);
+        float pv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const float za = (acc0[nt][0] + acc0[nt][1]) + (acc1[nt][0] + acc1[nt][1]);
-        if (all_local || local) z[nt] = za;
-      }
-    }
-
-    // Online softmax per head (column); the max used for the exponentials
-    // is raised only when it grows by more than kRescaleThreshold.
-    bool any_rescale = false;
-    float pr[kNT], al[kNT];
+        for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const bool valid = jstep + g < je && 4 * nt + t4 < GQ;
-      const float zz = valid ? z[nt] : -INFINITY;
-      float bm = zz;
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-      float alpha = 1.f;
-      if (bm > m_run[nt] + kRescaleThreshold) {
-        alpha = exp2f(m_run[nt] - bm);
-        m_run[nt] = bm;
-      }
-      const float mexp = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
-      pr[nt] = exp2f(zz - mexp);
-      l_run[nt] = l_run[nt] * alpha + pr[nt];
-      al[nt] = alpha;
-      any_rescale |= alpha != 1.f;
-    }
-    any_rescale = __any_sync(0xffffffffu, any_rescale);
-    if (any_rescale) {
-      // Column n of O^T belongs to head hcol(n); its alpha sits in lane
-      // hcol & 3 of n-tile hcol >> 2.
-      float ae = 1.f, ao = 1.f;
-      const int he = hcol(2 * t4), ho = hcol(2 * t4 + 1);
+          for (int r = 0; r < 2; ++r) {
+            const float a = __shfl_sync(0xffffffffu, pr[nt][r], src);
+            const float c = __shfl_sync(0xffffffffu, pr[nt][r], src + 4);
+            if ((hh >> 2) == nt) {
+              pv[r][0] = a;
+              pv[r][1] = c;
+            }
+          }
+        const bool use = hh < gq;
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const float x = __shfl_sync(0xffffffffu, al[nt], he & 3);
-        const float y = __shfl_sync(0xffffffffu, al[nt], ho & 3);
-        if ((he >> 2) == nt) ae = x;
-        if ((ho >> 2) == nt) ao = y;
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= ae;
-        o[mt][1] *= ao;
-        o[mt][2] *= ae;
-        o[mt][3] *= ao;
-      }
-    }
-    // P^T operand (B, 8 keys x 8 columns): keys 2 t4, 2 t4 + 1 of column g,
-    // i.e. of head hcol(g), from lanes 4 key + (head & 3) of n-tile head >> 2.
-    // P is split as hi + lo in bf16: with GQ <= 4 the lo parts fill columns
-    // 4..7, otherwise they go through a second product.
-    uint32_t pb_hi, pb_lo;
-    {
-      const int hh = hcol(g);
-      const int src = 8 * t4 + (hh & 3);
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const float a = __shfl_sync(0xffffffffu, pr[nt], src);
-        const float c = __shfl_sync(0xffffffffu, pr[nt], src + 4);
-        if ((hh >> 2) == nt) {
-          p0 = a;
-          p1 = c;
+        for (int r = 0; r < 2; ++r) {
+          uint32_t hi, lo;
+          split_bf16(make_float2(pv[r][0], pv[r][1]), hi, lo);
+          if constexpr (kLoCols) {
+            pb_hi[r] = use ? (g < 4 ? hi : lo) : 0u;
+            pb_lo[r] = 0u;
+          } else {
+            pb_hi[r] = use ? hi : 0u;
+            pb_lo[r] = use ? lo : 0u;
+          }
         }
       }
-      uint32_t hi, lo;
-      split_bf16(make_float2(p0, p1), hi, lo);
-      const bool use = hh < GQ;
-      if constexpr (kLoCols) {
-        pb_hi = use ? (g < 4 ? hi : lo) : 0u;
-        pb_lo = 0u;
-      } else {
-        pb_hi = use ? hi : 0u;
-        pb_lo = use ? lo : 0u;
-      }
-    }
-    // O^T += V^T P^T: four transposed 8x8 loads of V give the A operands of
-    // two 16-dim m-tiles each (keys past the slice end have p = 0 and
-    // zero-filled rows).
+      // O^T += V^T P^T: one transposed x4 load of V per 16-dim m-tile (keys
+      // past the slice end have p = 0 and zero-filled rows).
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      uint32_t v0, v1, v2, v3;
-      const int ch = 4 * jj + lm;
-      ldsm_x4_t(st + static_cast<uint32_t>((kStep + lr) * 256 + ((ch ^ lr) << 4)), v0, v1, v2, v3);
-      mma1688(o[2 * jj], v0, v1, pb_hi);
-      mma1688(o[2 * jj + 1], v2, v3, pb_hi);
-      if constexpr (!kLoCols) {
-        mma1688(o[2 * jj], v0, v1, pb_lo);
-        mma1688(o[2 * jj + 1], v2, v3, pb_lo);
+      for (int mt = 0; mt < kMT; ++mt) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(st + b_row + static_cast<uint32_t>(((2 * mt + b_hi) ^ b_sw) << 4), v0, v1, v2, v3);
+        mma16816(o[mt], v0, v1, v2, v3, pb_hi[0], pb_hi[1]);
+        if constexpr (!kLoCols) mma16816(o[mt], v0, v1, v2, v3, pb_lo[0], pb_lo[1]);
       }
     }
-    __syncwarp();  // the stage is rewritten next step
+    __syncwarp();  // the stage is rewritten next
+    issue_step(u + kStages);
   }
   cp_async_wait<0>();
 
@@ -520,118 +615,127 @@ decode_partial_kernel(DecodeKParams p) {
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     lh[nt] = l;
   }
-  // Each warp leaves its state in its (now idle) ring: o [GQ][128], then
-  // (m, l) [GQ][2]; the CTA then merges the warps of each KV head.
-  __syncthreads();
-  float* hand = reinterpret_cast<float*>(my_ring);
   if constexpr (kLoCols) {
     // Column n + 4 (lane t4 + 2) holds the lo-part product of column n.
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
   }
+  // Each warp leaves its state in its (now idle) ring: o [gq][D], then
+  // (m, l) [gq][2]; the CTA then merges the warps of each KV head.
+  __syncthreads();
+  float* hand = reinterpret_cast<float*>(my_ring);
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
+  for (int mt = 0; mt < kMT; ++mt) {
     const int d0 = 16 * mt + g;
     const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-    if (h0 < GQ) {
-      hand[h0 * kD + d0] = o[mt][0];
-      hand[h0 * kD + d0 + 8] = o[mt][2];
+    if (h0 < gq) {
+      hand[h0 * D + d0] = o[mt][0];
+      hand[h0 * D + d0 + 8] = o[mt][2];
     }
-    if (h1 < GQ) {
-      hand[h1 * kD + d0] = o[mt][1];
-      hand[h1 * kD + d0 + 8] = o[mt][3];
+    if (h1 < gq) {
+      hand[h1 * D + d0] = o[mt][1];
+      hand[h1 * D + d0 + 8] = o[mt][3];
     }
   }
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     const int h = 4 * nt + t4;
-    if (g == 0 && h < GQ) {
-      hand[GQ * kD + 2 * h] = m_run[nt];
-      hand[GQ * kD + 2 * h + 1] = lh[nt];
+    if (g == 0 && h < gq) {
+      hand[gq * D + 2 * h] = m_run[nt];
+      hand[gq * D + 2 * h + 1] = lh[nt];
     }
   }
   __syncthreads();
   // Merge: M = max over the head's warps, weights 2^(m_w - M).
-  for (int idx = tid; idx < p.Hq * 32; idx += nthr) {
-    const int hq = idx >> 5, d4 = idx & 31;
-    const int kv = hq / GQ, h = hq % GQ;
+  for (int idx = tid; idx < p.hpc * gq * kQuads; idx += nthr) {
+    const int hql = idx / kQuads, d4 = idx % kQuads;
+    const int kvl = hql / gq, h = hql % gq;
+    const int kv = hk0 + kvl;
+    if (kv >= p.Hkv) continue;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerHead; ++w) {
-      const float* src = reinterpret_cast<const float*>(s_ring + (kv + w * p.Hkv) * kStages * kStageBytes);
-      M = fmaxf(M, src[GQ * kD + 2 * h]);
+    for (int w = 0; w < wph; ++w) {
+      const float* src = reinterpret_cast<const float*>(s_ring + (kvl + w * p.hpc) * kStages * kStageBytes);
+      M = fmaxf(M, src[gq * D + 2 * h]);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerHead; ++w) {
-      const float* src = reinterpret_cast<const float*>(s_ring + (kv + w * p.Hkv) * kStages * kStageBytes);
-      const float mw = src[GQ * kD + 2 * h];
+    for (int w = 0; w < wph; ++w) {
+      const float* src = reinterpret_cast<const float*>(s_ring + (kvl + w * p.hpc) * kStages * kStageBytes);
+      const float mw = src[gq * D + 2 * h];
       const float a = M == -INFINITY ? 0.f : exp2f(mw - M);
-      lsum += a * src[GQ * kD + 2 * h + 1];
-      const float4 v = *reinterpret_cast<const float4*>(src + h * kD + 4 * d4);
+      lsum += a * src[gq * D + 2 * h + 1];
+      const float4 v = *reinterpret_cast<const float4*>(src + h * D + 4 * d4);
       acc.x += a * v.x;
       acc.y += a * v.y;
       acc.z += a * v.z;
       acc.w += a * v.w;
     }
-    const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + hq;
-    *reinterpret_cast<float4*>(p.part_o + slot * kD + 4 * d4) = acc;
-    if (d4 == 0) {
-      p.part_ml[slot * 2] = M;
-      p.part_ml[slot * 2 + 1] = lsum;
-    }
+    const long long slot = (static_cast<long long>(split) * p.B + b) * p.Hq + kv * gq + h;
+    *reinterpret_cast<float4*>(p.part_o + slot * D + 4 * d4) = acc;
+    if (d4 == 0) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(M, lsum);
   }
 }
 
 // Merge the per-slice partials of one (batch, query head) with log-sum-exp
 // weights: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max m_s.
-// One pass: each warp folds its slices (loaded four at a time, independent
-// loads) into a running (max, sum, vector); the eight warps combine in
-// shared memory.  A lane owns four output elements.
-__global__ void __launch_bounds__(256)
+// Each warp takes the slices s = warp (mod 16) and requests up to kBatch of
+// them at once (one round trip to L2 for up to 160 slices), folding them
+// into a running (max, sum, vector); the warps then combine in shared
+// memory.  A lane owns D / 32 output elements.
+constexpr int kMergeWarps = 16;
+constexpr int kMergeBatch = 10;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
 decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                     int nsplit, int BH, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float s_m[8], s_l[8];
-  __shared__ float4 s_acc[8][32];
+  constexpr int kV = D / 32;
+  __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
+  __shared__ __align__(16) float s_acc[kMergeWarps][D];
   // The partials are written by the preceding grid.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float M = -INFINITY, Lsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = warp; s0 < nsplit; s0 += 32) {
-    float ms[4], ls[4];
-    float4 os[4];
+  float acc[kV];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int s = s0 + 8 * k;
+  for (int v = 0; v < kV; ++v) acc[v] = 0.f;
+  for (int s0 = warp; s0 < nsplit; s0 += kMergeWarps * kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float os[kMergeBatch][kV];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const int s = s0 + kMergeWarps * k;
       if (s < nsplit) {
         const long long slot = static_cast<long long>(s) * BH + bh;
-        ms[k] = part_ml[slot * 2];
-        ls[k] = part_ml[slot * 2 + 1];
-        os[k] = *reinterpret_cast<const float4*>(part_o + slot * kD + 4 * lane);
+        ml[k] = *reinterpret_cast<const float2*>(part_ml + slot * 2);
+        if constexpr (kV == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(part_o + slot * D + 4 * lane);
+          os[k][0] = t.x; os[k][1] = t.y; os[k][2] = t.z; os[k][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(part_o + slot * D + 2 * lane);
+          os[k][0] = t.x; os[k][1] = t.y;
+        }
       } else {
-        ms[k] = -INFINITY;
-        ls[k] = 0.f;
-        os[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ml[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int v = 0; v < kV; ++v) os[k][v] = 0.f;
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float Mn = fmaxf(M, ms[k]);
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const float Mn = fmaxf(M, ml[k].x);
       if (Mn == -INFINITY) continue;
-      const float a = exp2f(M - Mn), w = exp2f(ms[k] - Mn);
-      Lsum = Lsum * a + ls[k] * w;
-      acc.x = acc.x * a + os[k].x * w;
-      acc.y = acc.y * a + os[k].y * w;
-      acc.z = acc.z * a + os[k].z * w;
-      acc.w = acc.w * a + os[k].w * w;
+      const float a = exp2f(M - Mn), w = exp2f(ml[k].x - Mn);
+      Lsum = Lsum * a + ml[k].y * w;
+#pragma unroll
+      for (int v = 0; v < kV; ++v) acc[v] = acc[v] * a + os[k][v] * w;
       M = Mn;
     }
   }
-  s_acc[warp][lane] = acc;
+#pragma unroll
+  for (int v = 0; v < kV; ++v) s_acc[warp][kV * lane + v] = acc[v];
   if (lane == 0) {
     s_m[warp] = M;
     s_l[warp] = Lsum;
@@ -640,106 +744,131 @@ decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
   if (warp == 0) {
     float Mt = s_m[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) Mt = fmaxf(Mt, s_m[w]);
-    float D = 0.f;
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 1; w < kMergeWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
+    float Dn = 0.f;
+    float t[kV];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int v = 0; v < kV; ++v) t[v] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
       const float a = s_m[w] == -INFINITY ? 0.f : exp2f(s_m[w] - Mt);
-      D += a * s_l[w];
-      const float4 v = s_acc[w][lane];
-      t.x += a * v.x;
-      t.y += a * v.y;
-      t.z += a * v.z;
-      t.w += a * v.w;
+      Dn += a * s_l[w];
+#pragma unroll
+      for (int v = 0; v < kV; ++v) t[v] += a * s_acc[w][kV * lane + v];
     }
-    const float inv = 1.f / D;
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + static_cast<long long>(bh) * kD + 4 * lane);
-    dst[0] = __floats2bfloat162_rn(t.x * inv, t.y * inv);
-    dst[1] = __floats2bfloat162_rn(t.z * inv, t.w * inv);
-    if (lse != nullptr && lane == 0) lse[bh] = (Mt + log2f(D)) * 0.69314718055994531f;
+    const float inv = 1.f / Dn;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + static_cast<long long>(bh) * D + kV * lane);
+#pragma unroll
+    for (int v = 0; v < kV; v += 2) dst[v / 2] = __floats2bfloat162_rn(t[v] * inv, t[v + 1] * inv);
+    if (lse != nullptr && lane == 0) lse[bh] = (Mt + log2f(Dn)) * 0.69314718055994531f;
   }
 }
 
+// Streaming multiprocessors of the current device (cached per device).
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
   }
-  return n;
+  return cache[dev];
+}
+
+// Capacity of the query-head template for gq query heads per KV head.
+int gq_capacity(int gq) { return gq <= 1 ? 1 : gq <= 2 ? 2 : gq <= 4 ? 4 : gq <= 8 ? 8 : 0; }
+
+template <int D, int GQ>
+cudaError_t launch_partial(const dim3& grid, int warps, size_t smem, const DecodeKParams& p, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<D, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  decode_partial_kernel<D, GQ><<<grid, 32 * warps, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 int decode_max_splits() { return kMaxSplits; }
 
+int decode_slice_cap() { return std::min(num_sms(), kMaxSplits); }
+
 size_t decode_workspace_bytes(int B, int Hq, int d, int Lcap) {
   (void)Lcap;
   return static_cast<size_t>(kMaxSplits) * B * Hq * (d + 2) * sizeof(float);
 }
 
+size_t decode_scratch_bytes(int B, int Hq, int d) {
+  return static_cast<size_t>(decode_slice_cap()) * B * Hq * (d + 2) * sizeof(float);
+}
+
+bool decode_supported(int Hq, int Hkv, int d) {
+  return (d == 64 || d == 128) && Hkv >= 1 && Hq % Hkv == 0 && gq_capacity(Hq / Hkv) != 0;
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.d != kD) return cudaErrorInvalidValue;
-  const int GQ = a.Hq / a.Hkv;
-  // Blocks per slice: enough slices for one wave over the SMs for one
-  // sequence; with a batch, up to kMinBlocksPerSplit blocks per slice as long
-  // as the batch's slices still fill a wave (short sequences would otherwise
-  // pay the per-CTA set-up for a single 64-key block).
-  const int nblocks = (a.L + kBlockKeys - 1) / kBlockKeys;
-  const int target = std::min(num_sms(), kMaxSplits);
-  const int fill = static_cast<int>(std::min<long long>(kMinBlocksPerSplit,
-                                                         static_cast<long long>(nblocks) * a.B / num_sms()));
-  const int bps = std::max((nblocks + target - 1) / target, fill);
-  const int nsplit = (nblocks + bps - 1) / bps;
+  if (!decode_supported(a.Hq, a.Hkv, a.d)) return cudaErrorInvalidValue;
+  const int gq = a.Hq / a.Hkv, cap = gq_capacity(gq);
+  const int ngroups = (a.Hkv + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
+  const int hpc = (a.Hkv + ngroups - 1) / ngroups;
+  const int wph = std::min(4, kMaxWarps / hpc);  // 1, 2 or 4: a table block is 4 steps
+  // Slices: one wave over the SMs for one sequence, in whole 16-key steps
+  // spread evenly; with a batch, up to kMinStepsPerSplit steps per slice as
+  // long as the batch's slices still fill a wave (short sequences would
+  // otherwise pay the per-CTA set-up for a few steps).
+  const int nsm = num_sms();
+  const int slice_cap = decode_slice_cap();
+  const long long S = (static_cast<long long>(a.L) + kStep - 1) / kStep;
+  const long long target = std::max(1, std::min(slice_cap, nsm / ngroups));
+  const long long fill = std::min<long long>(kMinStepsPerSplit, S * a.B * ngroups / nsm);
+  const long long sps = std::max((S + target - 1) / target, std::max(fill, 1LL));
+  const int nsplit = static_cast<int>((S + sps - 1) / sps);
 
   DecodeKParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
   p.vc = static_cast<const __nv_bfloat16*>(a.v_cache);
   p.part_o = a.part;
-  p.part_ml = a.part + static_cast<size_t>(kMaxSplits) * a.B * a.Hq * kD;
+  p.part_ml = a.part + static_cast<size_t>(slice_cap) * a.B * a.Hq * a.d;
   p.B = a.B; p.L = a.L; p.Lcap = a.Lcap; p.Hq = a.Hq; p.Hkv = a.Hkv;
-  p.w0 = a.w0; p.G = a.G; p.wp = a.wp; p.keys_per_split = bps * kBlockKeys;
+  p.gq = gq; p.hpc = hpc; p.wph = wph;
+  p.w0 = a.w0; p.G = a.G; p.wp = a.wp;
+  p.steps_base = static_cast<int>(S / nsplit);
+  p.steps_extra = static_cast<int>(S % nsplit);
   p.seqlens = a.seqlens;
   p.status = device_status_ptr();
   if (p.status == nullptr) return cudaErrorInvalidSymbol;
   p.scale_log2 = a.scale_log2;
   p.freqs = a.freqs;
 
-  const int warps = warps_per_head(GQ) * a.Hkv;
-  const size_t region_a = std::max(static_cast<size_t>(2) * a.Hq * kD * sizeof(float),    // q
-                                    static_cast<size_t>(kBlockKeys) * kTabStride * 16);     // rotation table
-  const size_t smem = region_a + static_cast<size_t>(8 + 9 + 1) * 64 * sizeof(float2) +   // R_-b, R_-8a, base
-                      static_cast<size_t>(warps) * kStages * kStageBytes;
+  const int warps = hpc * wph;
+  const size_t stage_bytes = static_cast<size_t>(kStep) * 2 * a.d * 2;
+  const size_t smem = static_cast<size_t>(2 * kBlockKeys + kSmallRows) * (a.d / 4) * 16 +  // tables
+                      static_cast<size_t>(3) * (a.d / 2) * sizeof(float2) +               // base, query rotations
+                      static_cast<size_t>(warps) * kStages * stage_bytes;                 // rings
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  const dim3 grid(nsplit, a.B);
-  cudaError_t err = cudaSuccess;
-#define JL_DECODE_CASE(GQV)                                                                      \
-  case GQV:                                                                                      \
-    err = cudaFuncSetAttribute(decode_partial_kernel<GQV>,                                       \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);          \
-    if (err != cudaSuccess) return err;                                                          \
-    decode_partial_kernel<GQV><<<grid, 32 * warps, smem, stream>>>(p);                           \
-    break;
-  switch (GQ) {
-    JL_DECODE_CASE(1)
-    JL_DECODE_CASE(2)
-    JL_DECODE_CASE(4)
-    JL_DECODE_CASE(8)
-    default:
-      return cudaErrorInvalidValue;
-  }
+  const dim3 grid(nsplit, a.B, ngroups);
+  cudaError_t err = cudaErrorInvalidValue;
+#define JL_DECODE_CASE(DV, GQV) \
+  if (a.d == DV && cap == GQV) err = launch_partial<DV, GQV>(grid, warps, smem, p, stream);
+  JL_DECODE_CASE(128, 1)
+  JL_DECODE_CASE(128, 2)
+  JL_DECODE_CASE(128, 4)
+  JL_DECODE_CASE(128, 8)
+  JL_DECODE_CASE(64, 1)
+  JL_DECODE_CASE(64, 2)
+  JL_DECODE_CASE(64, 4)
+  JL_DECODE_CASE(64, 8)
 #undef JL_DECODE_CASE
-  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   // The merge waits on the partial kernel through griddepcontrol.wait, so it
   // may be launched before that kernel finishes.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B * a.Hq);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -747,7 +876,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, static_cast<const float*>(p.part_o),
+  if (a.d == 128)
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, static_cast<const float*>(p.part_o),
+                              static_cast<const float*>(p.part_ml), nsplit, a.B * a.Hq,
+                              static_cast<__nv_bfloat16*>(a.o), a.lse);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, static_cast<const float*>(p.part_o),
                             static_cast<const float*>(p.part_ml), nsplit, a.B * a.Hq,
                             static_cast<__nv_bfloat16*>(a.o), a.lse);
 }

@@ -9,9 +9,11 @@
 // scratch array that is part of the library image instead of a caller
 // workspace.
 //
-// The array (kScratchBytes, 16 MiB: enough for B * Hq <= 63 at d = 128) is
-// a file-scope __device__ variable: every GPU on which the library is loaded
-// holds it until the process exits.  Host
+// The array (kScratchBytes, 16 MiB) is a file-scope __device__ variable:
+// every GPU on which the library is loaded holds it until the process exits.
+// A call needs min(SMs, 512) * B * Hq * (d + 2) * 4 bytes of it (one fp32
+// partial per key slice and query head), so on a 148-SM B300 it serves
+// B * Hq <= 218 at d = 128 and B * Hq <= 425 at d = 64.  Host
 // code cannot use the array's name as a device address, so the first call
 // on each device (with that device current) resolves the address with
 // cudaGetSymbolAddress and caches it; that first call should therefore be
@@ -30,8 +32,8 @@
 namespace jl {
 namespace {
 
-// 16 MiB: jl_bifocal_decode's workspace for B * Hq <= 63 query heads at
-// d = 128 (about 260 KiB per head).
+// 16 MiB: the per-slice partials of B * Hq <= 218 query heads at d = 128 on
+// a 148-SM GPU (one fp32 partial of d + 2 values per key slice and head).
 constexpr size_t kScratchBytes = size_t(16) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -71,10 +73,14 @@ int jl_bifocal_decode_noalloc(const void* q, const void* k_cache, const void* v_
                               int w_pretrained, double rope_theta, float softmax_scale,
                               void* cuda_stream) {
   using namespace jl;
-  if (B < 1 || Hq < 1 || d < 1 || Lcap < 1)
-    return set_error(JL_ERR_INVALID, "decode_noalloc: need B, Hq, d, Lcap >= 1");
-  const size_t need = jl_bifocal_decode_workspace_size(B, Hq, d, Lcap);
-  if (need == 0 || need > kScratchBytes) {
+  set_error(JL_OK, "");
+  // The same argument checks, in the same order, as jl_bifocal_decode; only
+  // then the size limit of the fixed array.
+  int rc = check_decode_args("decode_noalloc", q, k_cache, v_cache, L, Lcap, o, B, Hq, Hkv, d, w0, w_pretrained,
+                             rope_theta);
+  if (rc != JL_OK) return rc;
+  const size_t need = decode_scratch_bytes(B, Hq, d);
+  if (need > kScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg),
              "decode_noalloc: B=%d Hq=%d d=%d needs %zu bytes of scratch; the fixed array holds %zu",
@@ -89,9 +95,9 @@ int jl_bifocal_decode_noalloc(const void* q, const void* k_cache, const void* v_
              cudaGetErrorString(err));
     return set_error(JL_ERR_CUDA, msg);
   }
-  // Same validation and kernels as jl_bifocal_decode, on the fixed scratch.
-  return jl_bifocal_decode(q, k_cache, v_cache, L, Lcap, o, lse, B, Hq, Hkv, d, w0, w_pretrained,
-                           rope_theta, softmax_scale, scratch, need, cuda_stream);
+  // The kernels of jl_bifocal_decode, with the partials in the fixed array.
+  return decode_call("decode_noalloc", q, k_cache, v_cache, nullptr, L, Lcap, o, lse, B, Hq, Hkv, d, w0,
+                     w_pretrained, rope_theta, softmax_scale, static_cast<float*>(scratch), cuda_stream);
 }
 
 }  // extern "C"

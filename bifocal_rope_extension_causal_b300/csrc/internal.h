@@ -96,7 +96,15 @@ struct DecodeArgs {
   RopeFreqs freqs;
 };
 int decode_max_splits();
+// Largest number of key slices one decode launch uses on the current device:
+// min(SM count, decode_max_splits()).
+int decode_slice_cap();
+// Bytes of partials a decode call needs (device-independent upper bound) and
+// the tighter bound for the current device's slice cap.
 size_t decode_workspace_bytes(int B, int Hq, int d, int Lcap);
+size_t decode_scratch_bytes(int B, int Hq, int d);
+// Head layouts the decode kernels take: d in {64, 128}, Hq / Hkv in 1..8.
+bool decode_supported(int Hq, int Hkv, int d);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // ---- TMA descriptors (tma_host.cu) -------------------------------------------
@@ -105,9 +113,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
 
-// ---- Errors (api.cu) -----------------------------------------------------------
+// ---- Errors and shared checks (api.cu) -------------------------------------------
 // Record `msg` as this thread's jl_last_error() message; returns `code`.
 int set_error(int code, const char* msg);
+// Argument checks of the decode entry points (JL_OK, or the error code with
+// the message recorded); `who` prefixes the message.
+int check_decode_args(const char* who, const void* q, const void* k_cache, const void* v_cache, int L, int Lcap,
+                      const void* o, int B, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta);
+// Launches the decode kernels of a checked call with the partials at
+// `partials` (at least decode_scratch_bytes(B, Hq, d) bytes); JL_OK or
+// JL_ERR_CUDA with the message recorded.
+int decode_call(const char* who, const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                int L, int Lcap, void* o, float* lse, int B, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                double rope_theta, float softmax_scale, float* partials, void* cuda_stream);
 
 // ---- Device status word (api.cu) ----------------------------------------------
 // Device address of the library's status word; kernels with bounded waits set

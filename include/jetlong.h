@@ -242,7 +242,9 @@ size_t jl_bifocal_decode_workspace_size(int B, int Hq, int d, int Lcap);
  *           (1 <= L <= Lcap); G = jl_group_size(L, w_pretrained)
  *  o        bf16 [B, Hq, d]   output
  *  lse      fp32 [B, Hq]      natural-log LSE; may be NULL
- *  d        128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}; Hkv <= 8
+ *  d        64 or 128; Hkv >= 1 and Hq % Hkv == 0 with 1 <= Hq / Hkv <= 8
+ *           (query head h reads KV head h / (Hq / Hkv)); other layouts
+ *           return JL_ERR_UNSUPPORTED
  *  workspace >= jl_bifocal_decode_workspace_size(B, Hq, d, Lcap) bytes
  *
  *   local  (L-1 - j <= w0):  s_j = <R_{L-1} x_q, K_j>
@@ -282,9 +284,11 @@ int jl_bifocal_decode_varlen(const void* q, const void* k_cache, const void* v_c
  * Same arguments, semantics and kernels as jl_bifocal_decode minus the
  * workspace: the split-K partials live in a fixed 16 MiB scratch array that
  * is part of the library image (every GPU that loads the library holds it
- * until the process exits).  It serves B * Hq <= 63 at d = 128; larger sizes
- * return JL_ERR_UNSUPPORTED with a message.  The entry point itself calls no
- * allocator of any kind.
+ * until the process exits).  A call needs min(SM count, 512) * B * Hq *
+ * (d + 2) * 4 bytes of it, so on a 148-SM B300 it serves B * Hq <= 218 at
+ * d = 128 (B * Hq <= 425 at d = 64); larger sizes return JL_ERR_UNSUPPORTED
+ * with a message, after the same argument checks (and error codes) as
+ * jl_bifocal_decode.  The entry point itself calls no allocator of any kind.
  *  - The first call on each device (with that device current) resolves the
  *    scratch array's device address; make that first call before any stream
  *    capture.

@@ -165,14 +165,37 @@ def _decode_args(**kw):
     (dict(L=0), _capi.JL_ERR_INVALID),
     (dict(L=17), _capi.JL_ERR_INVALID),
     (dict(Hq=6, Hkv=4), _capi.JL_ERR_INVALID),
-    (dict(d=64), _capi.JL_ERR_UNSUPPORTED),
+    (dict(d=96), _capi.JL_ERR_UNSUPPORTED),
     (dict(Hq=48, Hkv=3), _capi.JL_ERR_UNSUPPORTED),
-    (dict(Hq=32, Hkv=16), _capi.JL_ERR_UNSUPPORTED),
+    (dict(Hq=64, Hkv=4), _capi.JL_ERR_UNSUPPORTED),
     (dict(ws=None), _capi.JL_ERR_WORKSPACE),
 ])
 def test_decode_argument_checks(lib, kw, code):
     assert lib.jl_bifocal_decode(*_decode_args(**kw)) == code
     assert lib.jl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(kc=None), dict(L=0), dict(L=17), dict(Hq=6, Hkv=4), dict(d=96), dict(Hq=48, Hkv=3),
+    dict(Hq=64, Hkv=4), dict(o=None, Hq=4096, Hkv=8), dict(Hkv=0, Hq=4096), dict(theta=0.0, Hq=4096),
+])
+def test_noalloc_decode_argument_checks_match_decode(lib, kw):
+    """The allocation-free decode rejects bad arguments with the same codes as
+    the workspace decode, before its scratch-size limit (the Hq = 4096 cases
+    would also exceed the fixed scratch array)."""
+    args = _decode_args(**kw)
+    want = lib.jl_bifocal_decode(*args)
+    assert want in (_capi.JL_ERR_INVALID, _capi.JL_ERR_UNSUPPORTED)
+    got = lib.jl_bifocal_decode_noalloc(*args[:15], args[17])
+    assert got == want, (kw, got, want)
+    assert lib.jl_last_error().decode()
+
+
+def test_decode_wider_shapes_pass_the_checks(lib):
+    """d = 64, 16 KV heads and 3, 5, 6 query heads per KV head reach the
+    workspace check (a small workspace is refused there, not the shape)."""
+    for kw in (dict(d=64), dict(Hq=32, Hkv=16), dict(Hq=3, Hkv=1), dict(Hq=40, Hkv=8), dict(Hq=12, Hkv=2)):
+        assert lib.jl_bifocal_decode(*_decode_args(wsb=16, **kw)) == _capi.JL_ERR_WORKSPACE, kw
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -46,20 +46,28 @@ def test_decode_workload_cache_invariant(jl):
         assert now == sums, "the KV cache was modified"
 
 
-@pytest.mark.parametrize("L,Lcap,Hq,Hkv,wp,w0", [
-    (1, 8, 4, 2, 4, 0),          # only the new token
-    (2, 2, 4, 4, 1, 0),          # G = 2, w0 = 0
-    (7, 40, 8, 1, 3, 2),         # ragged, G = 3, 8 query heads per KV head
-    (64, 64, 2, 2, 16, 5),       # exactly one 64-key block
-    (65, 100, 4, 1, 16, 0),      # one key past a block
-    (300, 300, 16, 8, 40, 17),   # G = 8, local/remote boundary inside a warp step
-    (1000, 1200, 32, 8, 300, 64),
-    (1000, 1000, 8, 8, 2000, 10),  # G = 1
-    (777, 800, 4, 2, 100, 776),  # w0 >= L-1: all local at G = 8
+@pytest.mark.parametrize("L,Lcap,Hq,Hkv,wp,w0,d", [
+    (1, 8, 4, 2, 4, 0, 128),          # only the new token
+    (2, 2, 4, 4, 1, 0, 128),          # G = 2, w0 = 0
+    (7, 40, 8, 1, 3, 2, 128),         # ragged, G = 3, 8 query heads per KV head
+    (64, 64, 2, 2, 16, 5, 128),       # exactly one 64-key block
+    (65, 100, 4, 1, 16, 0, 128),      # one key past a block
+    (300, 300, 16, 8, 40, 17, 128),   # G = 8, local/remote boundary inside a warp step
+    (1000, 1200, 32, 8, 300, 64, 128),
+    (1000, 1000, 8, 8, 2000, 10, 128),  # G = 1
+    (777, 800, 4, 2, 100, 776, 128),  # w0 >= L-1: all local at G = 8
+    (500, 512, 4, 2, 100, 30, 64),    # d = 64
+    (777, 800, 64, 8, 100, 20, 64),   # d = 64, 8 query heads per KV head
+    (2000, 2000, 16, 16, 500, 300, 64),  # d = 64, 16 KV heads (two head groups), MHA
+    (1000, 1000, 32, 16, 300, 64, 128),  # 16 KV heads (two head groups of 8)
+    (129, 200, 9, 9, 40, 3, 128),     # 9 KV heads: head groups of 5 and 4
+    (600, 650, 12, 4, 200, 50, 128),  # 3 query heads per KV head
+    (800, 800, 40, 8, 250, 100, 128),  # 5 query heads per KV head (Qwen3-14B layout)
+    (5000, 5000, 24, 4, 1000, 333, 64),  # 6 query heads per KV head, d = 64, G = 5
 ])
-def test_decode_small(jl, L, Lcap, Hq, Hkv, wp, w0):
-    kc, vc, qs = synth.decode_inputs(Lcap, Hq, Hkv, 128, L + 3 * w0, 1)
-    check_decode(jl, kc.cuda(), vc.cuda(), qs[0], L, w0, wp, 1e4, f"L={L} Hq={Hq} Hkv={Hkv}")
+def test_decode_small(jl, L, Lcap, Hq, Hkv, wp, w0, d):
+    kc, vc, qs = synth.decode_inputs(Lcap, Hq, Hkv, d, L + 3 * w0, 1)
+    check_decode(jl, kc.cuda(), vc.cuda(), qs[0], L, w0, wp, 1e4, f"L={L} Hq={Hq} Hkv={Hkv} d={d}")
 
 
 def test_decode_batch(jl):
@@ -67,11 +75,12 @@ def test_decode_batch(jl):
     check_decode(jl, kc.cuda(), vc.cuda(), qs[0], 450, 30, 100, 1e6, "B=3")
 
 
-def test_decode_matches_prefill_rows(jl):
+@pytest.mark.parametrize("d", [128, 64])
+def test_decode_matches_prefill_rows(jl, d):
     """Prefill fills the cache (k_rot_out); decode at length L' then agrees
     with prefill row L'-1 when both see the same G (here L' > w_p * (G-1))."""
     import torch
-    L, Hq, Hkv, d, wp, w0 = 700, 8, 2, 128, 200, 50
+    L, Hq, Hkv, wp, w0 = 700, 8, 2, 200, 50
     q, k, v = synth.prefill_inputs(L, Hq, Hkv, d, 21)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     krot = torch.empty_like(kd)
