@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
 
 #include <algorithm>
 #include <mutex>
@@ -13,6 +14,7 @@
 #include "../../include/jetlong.h"
 #include "internal.h"
 #include "positions.cuh"
+#include "rope_math.cuh"
 
 namespace jl {
 
@@ -57,6 +59,29 @@ RopeFreqs make_rope_freqs(int d, double theta) {
   RopeFreqs f{};
   for (int i = 0; i < d / 2 && i < kMaxHalfDim; ++i) f.w[i] = pow(theta, -2.0 * i / d);
   return f;
+}
+
+AngleTable make_angle_table(int d, double theta) {
+  AngleTable t{};
+  const RopeFreqs f = make_rope_freqs(d, theta);
+  for (int i = 0; i < d / 2 && i < kMaxHalfDim; ++i) {
+    for (int l = 0; l < 3; ++l) {
+      // x = 2^(10 l) omega exactly; r = x mod 2 pi in [-pi, pi], with 2 pi as
+      // the nearest double plus its remainder (each fma rounds once).
+      const double x = ldexp(f.w[i], 10 * l);
+      const double m = rint(x / kTwoPiHi);
+      double r = fma(-m, kTwoPiHi, x);
+      r = fma(-m, kTwoPiLo, r);
+      uint32_t bits;
+      float hi = static_cast<float>(r);
+      memcpy(&bits, &hi, 4);
+      bits &= 0xfffffc00u;  // 14 significant bits
+      memcpy(&hi, &bits, 4);
+      t.hi[l][i] = hi;
+      t.lo[l][i] = static_cast<float>(r - static_cast<double>(hi));
+    }
+  }
+  return t;
 }
 
 }  // namespace jl
@@ -575,7 +600,7 @@ int decode_call(const char* who, const void* q, const void* k_cache, const void*
   a.G = static_cast<int>(jl::group_size(L, w_pretrained));
   a.wp = w_pretrained;
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
-  a.freqs = make_rope_freqs(d, rope_theta);
+  a.ang = make_angle_table(d, rope_theta);
   const cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return fail(JL_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return JL_OK;

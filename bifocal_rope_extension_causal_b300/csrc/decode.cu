@@ -7,8 +7,11 @@
 // R_{f(j)} x_j, while the query is rotated at f(q) (Delta_q = f(q) - q).
 //
 // Work split.  The key range [0, L) is cut into `nsplit` contiguous slices of
-// whole 16-key steps, as even as the step count allows, one CTA each and
-// about one per SM; a CTA covers up to eight KV heads of its slice (more KV
+// whole 16-key steps, one CTA each and about one per SM.  Steps that hold
+// remote keys (a prefix of [0, L)) cost more than all-local steps (they
+// take the correction rotation), so the slices are balanced by cost: the
+// first n_r slices share the remote steps evenly and the rest share the
+// local ones.  A CTA covers up to eight KV heads of its slice (more KV
 // heads take more CTAs along grid z), so the per-key rotation table is built
 // once and shared by all of its heads.  Each CTA writes an unnormalised
 // partial (running max m, sum l, sum p v) per query head; a second kernel,
@@ -46,8 +49,9 @@
 // slice start j0 = js + 64 b.  Within a block, key j0 + t needs
 // R_{Delta(j0+t)} = R_{Delta(j0)} R_{-n(t)}, n(t) = t - (f(j0+t) - f(j0)) in
 // [0, 63], and R_{-n} = R_{-8a} R_{-c} (n = 8a + c) comes from two small
-// per-CTA tables.  The block base R_{Delta(j0)} is reduced in double
-// precision once per CTA and then stepped block to block by R_{-n64},
+// per-CTA tables.  The block base R_{Delta(j0)} is reduced accurately (float
+// arithmetic on host-reduced angle tables, no fp64) once per CTA and then
+// stepped block to block by R_{-n64},
 // n64 = 64 - (f(j0+64) - f(j0)).  Each thread owns one frequency pair of the
 // table and keeps that pair's base in registers.  The tables of two blocks
 // are double-buffered: while the warps stream block b they build block b+1's
@@ -72,6 +76,7 @@ constexpr int kMaxWarps = 8;
 constexpr int kMaxSplits = 512;
 constexpr int kMinStepsPerSplit = 32;  // batched decode: steps per slice when the batch fills the SMs
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr double kRemoteCost = 1.6;        // cost of a step with remote keys / an all-local step
 constexpr int kSmallRows = 17;             // R_{-c} (c < 8), then R_{-8a} (a <= 8)
 
 struct DecodeKParams {
@@ -83,10 +88,54 @@ struct DecodeKParams {
   int* status;     // device status word
   const int* seqlens;  // per-sequence lengths [B] (device) or nullptr: every sequence has length L
   int B, L, Lcap, Hq, Hkv, gq, hpc, wph, w0, G, wp;
-  int steps_base, steps_extra;  // slice s holds steps_base + (s < steps_extra) 16-key steps
+  // Slices s < split_r share steps [0, steps_r) evenly, the others share
+  // [steps_r, steps_all); with per-sequence lengths, steps past a
+  // sequence's end are empty.
+  int steps_r, steps_all, split_r;
   float scale_log2;
-  RopeFreqs freqs;
+  AngleTable ang;
 };
+
+// 2 pi as three floats: P1 keeps 13 significant bits, so that k * P1 is
+// exact for |k| <= 1024.
+constexpr float kTwoPiP1 = 6.283203125f;
+constexpr float kTwoPiP2 = -1.781781975296326e-05f;
+constexpr float kTwoPiP3 = -6.605598229861287e-13f;
+constexpr float kInvTwoPiF = 0.15915494309189535f;
+
+// cos and sin of n * omega_i for |n| < 2^30 in float arithmetic only (the
+// fp64 pipe is slow on this GPU).  With n = d2 2^20 + d1 2^10 + d0 (10-bit
+// digits), n omega = sum_l d_l phi_l mod 2 pi, phi_l from the host's table:
+// d_l * hi_l is exact, is reduced by 2 pi = P1 + P2 + P3 (k * P1 exact),
+// and the reduced heads are summed without rounding error (two-sum) while
+// the small tails (d_l * lo_l, k * P2, k * P3) accumulate separately.  The
+// angle handed to sincosf is within about 1.5e-7 rad of the exact one.
+// `hi` and `lo` point to the table staged in shared memory ([3][kMaxHalfDim]
+// each): kernel parameters indexed differently in every lane serialise.
+__device__ __forceinline__ float2 rope_cos_sin_f(long long n, const float* hi, const float* lo, int i) {
+  const bool neg = n < 0;
+  const unsigned int m = static_cast<unsigned int>(neg ? -n : n);
+  float sh = 0.f, sl = 0.f;
+#pragma unroll
+  for (int l = 0; l < 3; ++l) {
+    const float d = static_cast<float>((m >> (10 * l)) & 1023u);
+    const float tt = d * hi[l * kMaxHalfDim + i];  // exact
+    const float k = rintf(tt * kInvTwoPiF);
+    const float rh = fmaf(-k, kTwoPiP1, tt);  // exact
+    const float s = sh + rh, bb = s - sh;
+    sl += (sh - (s - bb)) + (rh - bb);
+    sh = s;
+    sl = fmaf(-k, kTwoPiP2, sl);
+    sl = fmaf(-k, kTwoPiP3, sl);
+    sl = fmaf(d, lo[l * kMaxHalfDim + i], sl);
+  }
+  const float k = rintf(sh * kInvTwoPiF);
+  sh = fmaf(-k, kTwoPiP1, sh);
+  sl = fmaf(-k, kTwoPiP2, sl);
+  float sn, cs;
+  sincosf(sh + sl, &sn, &cs);
+  return make_float2(cs, neg ? -sn : sn);
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
@@ -198,6 +247,7 @@ decode_partial_kernel(DecodeKParams p) {
   float2* s_qcs = s_base0 + kHalf;                                              // [2][kHalf]
   unsigned char* s_ring = reinterpret_cast<unsigned char*>(s_qcs + 2 * kHalf);
   const __nv_bfloat16* s_q = reinterpret_cast<const __nv_bfloat16*>(s_tab + kTabEntries);
+  __shared__ float s_ang_hi[3 * kMaxHalfDim], s_ang_lo[3 * kMaxHalfDim];  // the angle tables, staged
 
   // Let the merge kernel (a programmatic dependent) launch early; it waits
   // for this grid's completion before reading the partials.
@@ -218,10 +268,17 @@ decode_partial_kernel(DecodeKParams p) {
     }
     G = static_cast<int>(group_size(L, p.wp));
   }
-  const long long step0 = static_cast<long long>(split) * p.steps_base + min(split, p.steps_extra);
-  const long long nstep_slice = p.steps_base + (split < p.steps_extra ? 1 : 0);
+  long long step0, step1;
+  if (split < p.split_r) {
+    step0 = static_cast<long long>(p.steps_r) * split / p.split_r;
+    step1 = static_cast<long long>(p.steps_r) * (split + 1) / p.split_r;
+  } else {
+    const long long nl = gridDim.x - p.split_r, sl = split - p.split_r, rest = p.steps_all - p.steps_r;
+    step0 = p.steps_r + rest * sl / nl;
+    step1 = p.steps_r + rest * (sl + 1) / nl;
+  }
   const int js = static_cast<int>(min(static_cast<long long>(L), kStep * step0));
-  const int je = static_cast<int>(min(static_cast<long long>(L), kStep * (step0 + nstep_slice)));
+  const int je = static_cast<int>(min(static_cast<long long>(L), kStep * step1));
   const int qpos = L - 1;
   const bool bifocal = G > 1;
   const int first_local = qpos - p.w0;  // keys j >= first_local are local
@@ -290,6 +347,12 @@ decode_partial_kernel(DecodeKParams p) {
   };
 #pragma unroll
   for (int s = 0; s < kStages; ++s) issue_step(s);
+  for (int i = tid; i < 3 * kHalf; i += nthr) {
+    const int l = i / kHalf, f = i % kHalf;
+    s_ang_hi[l * kMaxHalfDim + f] = p.ang.hi[l][f];
+    s_ang_lo[l * kMaxHalfDim + f] = p.ang.lo[l][f];
+  }
+  __syncthreads();
 
   // ---- Set-up, while the query rows and the first two steps are in flight ----
   // Query rotations R_{L-1} and R_{f(L-1)}, the first block's base
@@ -300,7 +363,7 @@ decode_partial_kernel(DecodeKParams p) {
   for (int i = tid; i < kHalf * (any_remote ? 3 : 2); i += nthr) {
     const int which = i / kHalf, f = i % kHalf;
     const long long pos = which == 0 ? qpos : which == 1 ? alias(qpos, G) : alias_offset(js, G);
-    const float2 cs = rope_cos_sin(pos, p.freqs.w[f]);
+    const float2 cs = rope_cos_sin_f(pos, s_ang_hi, s_ang_lo, f);
     if (which < 2)
       s_qcs[which * kHalf + f] = cs;
     else
@@ -310,17 +373,8 @@ decode_partial_kernel(DecodeKParams p) {
     for (int idx = tid; idx < kSmallRows * kQuads; idx += nthr) {
       const int r = idx / kQuads, pp = idx % kQuads;
       const int n = r < 8 ? r : 8 * (r - 8);
-      float2 cs[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const double w = p.freqs.w[2 * pp + k];
-        const float whi = __uint_as_float(__float_as_uint(static_cast<float>(w)) & 0xffffff80u);
-        const float wlo = static_cast<float>(w - static_cast<double>(whi));
-        float sn, cn;
-        sincosf(static_cast<float>(n) * whi, &sn, &cn);
-        const float e = static_cast<float>(n) * wlo;  // |e| < 1e-3
-        cs[k] = compose(make_float2(cn, sn), make_float2(1.f - 0.5f * e * e, e));
-      }
+      const float2 cs[2] = {rope_cos_sin_f(n, s_ang_hi, s_ang_lo, 2 * pp),
+                            rope_cos_sin_f(n, s_ang_hi, s_ang_lo, 2 * pp + 1)};
       s_small[idx] = make_float4(cs[0].x, cs[1].x, -cs[0].y, -cs[1].y);  // R_{-n}
     }
   }
@@ -622,8 +676,32 @@ decode_partial_kernel(DecodeKParams p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
   }
-  // Each warp leaves its state in its (now idle) ring: o [gq][D], then
-  // (m, l) [gq][2]; the CTA then merges the warps of each KV head.
+  if (wph == 1) {
+    // One warp per KV head: its state is the CTA's partial for the head.
+    if (!head_ok) return;
+    const long long slot0 = (static_cast<long long>(split) * p.B + b) * p.Hq + hk * gq;
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+      const int d0 = 16 * mt + g;
+      const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+      if (h0 < gq) {
+        p.part_o[(slot0 + h0) * D + d0] = o[mt][0];
+        p.part_o[(slot0 + h0) * D + d0 + 8] = o[mt][2];
+      }
+      if (h1 < gq) {
+        p.part_o[(slot0 + h1) * D + d0] = o[mt][1];
+        p.part_o[(slot0 + h1) * D + d0 + 8] = o[mt][3];
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int h = 4 * nt + t4;
+      if (g == 0 && h < gq) *reinterpret_cast<float2*>(p.part_ml + (slot0 + h) * 2) = make_float2(m_run[nt], lh[nt]);
+    }
+    return;
+  }
+  // Several warps per KV head: each leaves its state in its (now idle)
+  // ring, o [gq][D] then (m, l) [gq][2], and the CTA merges them.
   __syncthreads();
   float* hand = reinterpret_cast<float*>(my_ring);
 #pragma unroll
@@ -835,13 +913,37 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.B = a.B; p.L = a.L; p.Lcap = a.Lcap; p.Hq = a.Hq; p.Hkv = a.Hkv;
   p.gq = gq; p.hpc = hpc; p.wph = wph;
   p.w0 = a.w0; p.G = a.G; p.wp = a.wp;
-  p.steps_base = static_cast<int>(S / nsplit);
-  p.steps_extra = static_cast<int>(S % nsplit);
+  // Cost split: steps holding a remote key cost about kRemoteCost times an
+  // all-local step (correction rotation and hi/lo split of every element,
+  // measured on B300 at L = 32769).  Batched decode with per-sequence
+  // lengths keeps the even split (each sequence has its own G and window).
+  long long steps_r = S;
+  if (a.seqlens == nullptr) {
+    const long long first_local = static_cast<long long>(a.L) - 1 - a.w0;  // keys >= first_local are local
+    steps_r = a.G > 1 ? std::min(S, std::max(0LL, (first_local + kStep - 1) / kStep)) : 0;
+  }
+  int split_r = nsplit;
+  if (steps_r < S) {
+    const double wr = kRemoteCost * static_cast<double>(steps_r), wl = static_cast<double>(S - steps_r);
+    split_r = static_cast<int>(std::lround(nsplit * wr / (wr + wl)));
+    split_r = std::max(steps_r > 0 ? 1 : 0, std::min(split_r, nsplit - 1));
+  }
+  // One region when either side gets no slice (e.g. a single slice).
+  if (split_r >= nsplit) {
+    split_r = nsplit;
+    steps_r = S;
+  } else if (split_r <= 0) {
+    split_r = 0;
+    steps_r = 0;
+  }
+  p.steps_r = static_cast<int>(steps_r);
+  p.steps_all = static_cast<int>(S);
+  p.split_r = split_r;
   p.seqlens = a.seqlens;
   p.status = device_status_ptr();
   if (p.status == nullptr) return cudaErrorInvalidSymbol;
   p.scale_log2 = a.scale_log2;
-  p.freqs = a.freqs;
+  p.ang = a.ang;
 
   const int warps = hpc * wph;
   const size_t stage_bytes = static_cast<size_t>(kStep) * 2 * a.d * 2;

@@ -16,6 +16,16 @@ struct RopeFreqs {
 };
 RopeFreqs make_rope_freqs(int d, double theta);
 
+// Per-frequency angle tables for float-only rotary angles (decode): level l
+// holds phi_l = (2^(10 l) omega_i) mod 2 pi, reduced in double on the host
+// and split as hi + lo, hi keeping 14 significant bits so that d * hi is
+// exact in float for any 10-bit integer d.
+struct AngleTable {
+  float hi[3][kMaxHalfDim];
+  float lo[3][kMaxHalfDim];
+};
+AngleTable make_angle_table(int d, double theta);
+
 // A bf16 tensor addressed as [B, H, rows, d]: element (b, h, row, e) lives at
 // base + b * sb + h * sh + row * sr + e (strides in elements).  Head-major
 // workspace tensors [B, H, L, d] and cache-layout tensors [B, Lcap, H, d]
@@ -93,7 +103,7 @@ struct DecodeArgs {
   const int* seqlens;   // per-sequence lengths [B] on the device, or nullptr
   int B, L, Lcap, Hq, Hkv, d, w0, G, wp;  // L: the length, or the largest one with seqlens
   float scale_log2;
-  RopeFreqs freqs;
+  AngleTable ang;
 };
 int decode_max_splits();
 // Largest number of key slices one decode launch uses on the current device:
