@@ -98,6 +98,14 @@ SIGNATURES = {
     "jl_bifocal_decode_noalloc_scratch_bytes": (_c.c_size_t, []),
     "jl_device_status": (_c.c_int, [_c.c_void_p]),
     "jl_selftest_bounded_wait": (_c.c_int, [_c.c_longlong, _c.c_void_p]),
+    "jl_selftest_prefill_wait_limit": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k, v
+        _c.c_void_p, _c.c_void_p,                          # o, lse
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,  # B, L, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_double,                   # w0, w_pretrained, theta
+        _c.c_longlong,                                     # limit_cycles
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_last_error": (_c.c_char_p, []),
 }
 

@@ -176,10 +176,14 @@ int jl_bifocal_rope(const void* q, const void* k, int B, int L, int Hq, int Hkv,
   return JL_OK;
 }
 
-int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d,
-                         int w0, int w_pretrained, float softmax_scale, const void* workspace,
-                         size_t workspace_bytes, void* cuda_stream) {
-  t_err[0] = '\0';
+}  // extern "C"
+
+namespace {
+
+// jl_bifocal_attention with a given pipeline wait limit (0: the default).
+int attention_call(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d, int w0,
+                   int w_pretrained, float softmax_scale, const void* workspace, size_t workspace_bytes,
+                   long long wait_limit, void* cuda_stream) {
   if (!v || !o) return fail(JL_ERR_INVALID, "attention: null v/o pointer");
   int rc = check_prefill_shape("attention", B, L, Hq, Hkv, d, w0, w_pretrained);
   if (rc != JL_OK) return rc;
@@ -199,9 +203,37 @@ int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int H
   a.o = o; a.lse = lse;
   a.B = B; a.Lq = L; a.Lk = L; a.q_base = 0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
+  a.wait_limit = wait_limit;
   const cudaError_t e = launch_prefill_attention(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention: kernel launch");
   return JL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d,
+                         int w0, int w_pretrained, float softmax_scale, const void* workspace,
+                         size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, softmax_scale, workspace, workspace_bytes,
+                        0, cuda_stream);
+}
+
+int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                   int L, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta,
+                                   long long limit_cycles, void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream) {
+  t_err[0] = '\0';
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL)
+    return fail(JL_ERR_INVALID, "selftest: limit_cycles must be in [1, 4e9]");
+  if (!q || !k || !v || !o) return fail(JL_ERR_INVALID, "selftest: null q/k/v/o pointer");
+  int rc = jl_bifocal_rope(q, k, B, L, Hq, Hkv, d, w_pretrained, rope_theta, nullptr, workspace,
+                           workspace_bytes, cuda_stream);
+  if (rc != JL_OK) return rc;
+  return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, 0.f, workspace, workspace_bytes,
+                        limit_cycles, cuda_stream);
 }
 
 int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,

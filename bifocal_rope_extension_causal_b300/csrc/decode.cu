@@ -281,7 +281,6 @@ decode_partial_kernel(DecodeKParams p) {
   const int je = static_cast<int>(min(static_cast<long long>(L), kStep * step1));
   const int qpos = L - 1;
   const bool bifocal = G > 1;
-  const int first_local = qpos - p.w0;  // keys j >= first_local are local
 
   // Warp `par` of KV head hkl takes the global steps it = wph * u + par.
   // KV heads past Hkv (last head group) stream nothing but keep the CTA's
@@ -359,7 +358,7 @@ decode_partial_kernel(DecodeKParams p) {
   // R_{Delta(js)} (angles reduced in double), and the small tables R_{-c}
   // (c < 8) and R_{-8a} (a <= 8) with omega = hi + lo, hi holding 17
   // significant bits so that n * hi is exact in float for n <= 64.
-  const bool any_remote = bifocal && js < first_local && js < je;
+  const bool any_remote = bifocal && js < je && !is_local(qpos, js, p.w0);
   for (int i = tid; i < kHalf * (any_remote ? 3 : 2); i += nthr) {
     const int which = i / kHalf, f = i % kHalf;
     const long long pos = which == 0 ? qpos : which == 1 ? alias(qpos, G) : alias_offset(js, G);
@@ -477,7 +476,7 @@ decode_partial_kernel(DecodeKParams p) {
     // after this barrier nobody reads block blk - 1's buffer any more.
     if (ub == 0 && blk > 0) __syncthreads();
     // Part of the next block's table (remote keys form a prefix of [0, L)).
-    if (bifocal && j0 + kBlockKeys < first_local && j0 + kBlockKeys < je) {
+    if (bifocal && j0 + kBlockKeys < je && !is_local(qpos, j0 + kBlockKeys, p.w0)) {
       if (ub == 0) {  // base and residue of block blk + 1
         const int q64 = div_small(r0 + kBlockKeys, G, invG);
         const int n = kBlockKeys - q64;  // 0..64
@@ -492,8 +491,8 @@ decode_partial_kernel(DecodeKParams p) {
     if (it < nsteps) {
       const int jstep = js + it * kStep;
       const uint32_t st = ring + static_cast<uint32_t>((u & (kStages - 1)) * kStageBytes);
-      const bool all_local = !bifocal || jstep >= first_local;
-      const bool all_remote = bifocal && jstep + kStep - 1 < first_local;
+      const bool all_local = !bifocal || is_local(qpos, jstep, p.w0);
+      const bool all_remote = bifocal && !is_local(qpos, jstep + kStep - 1, p.w0);
 
       // Scores z[nt][r] of (key jstep + g + 8 r, head 4 nt + t4), log2 units.
       float z[kNT][2];
@@ -919,7 +918,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // lengths keeps the even split (each sequence has its own G and window).
   long long steps_r = S;
   if (a.seqlens == nullptr) {
-    const long long first_local = static_cast<long long>(a.L) - 1 - a.w0;  // keys >= first_local are local
+    const long long first_local = first_local_key(a.L - 1, a.w0);  // keys >= first_local are local
     steps_r = a.G > 1 ? std::min(S, std::max(0LL, (first_local + kStep - 1) / kStep)) : 0;
   }
   int split_r = nsplit;

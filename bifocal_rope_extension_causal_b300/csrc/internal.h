@@ -81,6 +81,10 @@ struct PrefillArgs {
   // Window-only mode (the local views of the three-pass form): score only
   // the pairs with 0 <= q - k <= w0, with the qa/ka rotations.
   bool window_only = false;
+  // Clock cycles a pipeline wait may take before the CTA gives up (records a
+  // status code and skips its remaining work); 0 selects the default
+  // (about 2 s).  Only the test-support entry point sets it.
+  long long wait_limit = 0;
 };
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 

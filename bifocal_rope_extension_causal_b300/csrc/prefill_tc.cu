@@ -72,6 +72,7 @@ struct Cfg {
 struct TcParams {
   int B, Lq, q_base, Hq, Hkv, w0, G, npairs;
   int window_only;  // skip the remote phase (local views of the three-pass form)
+  long long wait_limit;  // clock cycles a pipeline wait may take before the CTA gives up
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -90,10 +91,8 @@ __device__ __forceinline__ Plan make_plan(int q0, int qend, int w0, bool window_
   Plan p;
   const int qlast = min(q0 + 2 * kBM - 1, qend - 1);
   p.jmax = qlast / kBN;
-  const int t = qlast - w0 - 1;  // remote pairs with key tile j iff kBN * j <= t
-  p.nr = (t >= 0 && !window_only) ? min(t / kBN, p.jmax) + 1 : 0;
-  const int u = q0 - (kBN - 1) - w0;  // local pairs with key tile j iff kBN * j >= u
-  p.jl0 = u <= 0 ? 0 : (u + kBN - 1) / kBN;
+  p.nr = window_only ? 0 : min(remote_tile_count(qlast, w0, kBN), p.jmax + 1);
+  p.jl0 = first_local_tile(q0, w0, kBN);
   p.nv = p.nr + (p.jmax - p.jl0 + 1);
   return p;
 }
@@ -185,6 +184,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
             tma_load_4d(sQ + t * kTileBytes + c * kBoxBytes, m, bar(bars.q_full), 64 * c, h, row0 + t * kBM, b);
       };
       load_q(plan.nr > 0 ? &tm_qr : &tm_qa);
+      int qloads = 1;
       bool ok = true;
       int idx = 0;
       for (int v = 0; v < plan.nv && ok; ++v) {
@@ -192,12 +192,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
         bool remote;
         visit_of(plan, v, j, remote);
         if (v == plan.nr && v > 0) {  // switch the resident Q rotation
-          if (!(ok = mbar_wait(bar(bars.q_empty), 0, &s_abort, kWaitLimit))) { fail(1); break; }
+          if (!(ok = mbar_wait(bar(bars.q_empty), 0, &s_abort, prm.wait_limit))) { fail(1); break; }
           load_q(&tm_qa);
+          ++qloads;
         }
         for (int part = 0; part < 2 && ok; ++part, ++idx) {  // K then V
           const int s = idx % kSlots, use = idx / kSlots;
-          if (use > 0 && !(ok = mbar_wait(bar(bars.empty[s]), (use - 1) & 1, &s_abort, kWaitLimit))) {
+          if (use > 0 && !(ok = mbar_wait(bar(bars.empty[s]), (use - 1) & 1, &s_abort, prm.wait_limit))) {
             fail(2);
             break;
           }
@@ -209,22 +210,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
           }
         }
       }
+      // Drain: every bulk copy this thread started has landed before the CTA
+      // may exit (on the normal path these waits return at once).  The
+      // latest arming of each ring slot is among the last kSlots loads; the
+      // waits use the full limit and ignore the abort flag.
+      const volatile int never = 0;
+      bool drained = true;
+      for (int i = max(0, idx - kSlots); i < idx; ++i)
+        drained &= mbar_wait(bar(bars.full[i % kSlots]), (i / kSlots) & 1, &never, kWaitLimit);
+      drained &= mbar_wait(bar(bars.q_full), (qloads - 1) & 1, &never, kWaitLimit);
+      if (!drained) atomicCAS(prm.status, 0, 11);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issue
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false);
       const uint32_t id_pv = idesc_bf16_f32(kBM, D, true);
-      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, kWaitLimit);
+      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, prm.wait_limit);
       if (!ok) fail(3);
       auto wait_slot = [&](int idx) {
         const int s = idx % kSlots;
-        if (!mbar_wait(bar(bars.full[s]), (idx / kSlots) & 1, &s_abort, kWaitLimit)) { fail(4); return false; }
+        if (!mbar_wait(bar(bars.full[s]), (idx / kSlots) & 1, &s_abort, prm.wait_limit)) { fail(4); return false; }
         tc_fence_after();
         return true;
       };
       auto pv = [&](int t, int vprev) {  // O_t += P_t V(vprev)
-        if (!mbar_wait(bar(bars.p_full[t]), vprev & 1, &s_abort, kWaitLimit)) { fail(5); return false; }
+        if (!mbar_wait(bar(bars.p_full[t]), vprev & 1, &s_abort, prm.wait_limit)) { fail(5); return false; }
         tc_fence_after();
         const uint32_t vs = sRing + ((2 * vprev + 1) % kSlots) * kTileBytes;
         for (int kk = 0; kk < kBN / 16; ++kk)
@@ -244,7 +255,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
             if (t == 1) mma_commit(bar(bars.empty[(2 * (v - 1) + 1) % kSlots]));
           }
           if (t == 0 && v == plan.nr && v > 0) {  // first local visit: Q_abs resident?
-            if (!(ok = mbar_wait(bar(bars.q_full), 1, &s_abort, kWaitLimit))) { fail(6); break; }
+            if (!(ok = mbar_wait(bar(bars.q_full), 1, &s_abort, prm.wait_limit))) { fail(6); break; }
             tc_fence_after();
           }
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -289,7 +300,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
       bool remote;
       visit_of(plan, v, j, remote);
       const int k0 = j * kBN;
-      if (!(ok = mbar_wait(bar(bars.s_full[t]), v & 1, &s_abort, kWaitLimit))) { fail(8); break; }
+      // Every lane waits; the outcome is made warp-uniform, since the
+      // tensor-memory accesses that follow are warp-collective.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[t]), v & 1, &s_abort, prm.wait_limit));
+      if (!ok) { fail(8); break; }
       tc_fence_after();
       uint32_t a0[32], a1[32], a2[32], a3[32];
       tmem_ld32(tS + 0, a0);
@@ -309,15 +323,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
         s[96 + i] = __uint_as_float(a3[i]);
       }
       // Masks are needed only on tiles at the window band or the diagonal.
-      const bool need_mask = remote ? (q0t - (k0 + kBN - 1) <= w0)
-                                    : ((q0t + kBM - 1 - k0 > w0) || (k0 + kBN - 1 > q0t));
+      const bool need_mask = remote ? remote_visit_needs_mask(q0t, kBM, k0, kBN, w0)
+                                    : local_visit_needs_mask(q0t, kBM, k0, kBN, w0);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int dist = q - (k0 + c);
-          const bool keep = remote ? (dist > w0) : (dist >= 0 && dist <= w0);
-          if (!keep) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (!visit_keeps(remote, q, k0 + c, w0)) s[c] = -INFINITY;
       }
       // Row max and row sum as 8-way trees (independent chains).
       float mx8[8];
@@ -361,7 +372,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
       tmem_st32(tS + 32, pk1);
       // Rescale O_t in tensor memory when any row of this warp raised its max.
       if (v > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-        if (!(ok = mbar_wait(bar(bars.pv_done[t]), (v - 1) & 1, &s_abort, kWaitLimit))) { fail(9); break; }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.pv_done[t]), (v - 1) & 1, &s_abort, prm.wait_limit));
+        if (!ok) { fail(9); break; }
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -377,7 +389,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(bars.p_full[t]));
     }
-    if (ok && mbar_wait(bar(bars.pv_done[t]), (plan.nv - 1) & 1, &s_abort, kWaitLimit)) {
+    // P stores of an iteration that gave up may still be in flight.
+    tmem_st_wait();
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.pv_done[t]), (plan.nv - 1) & 1, &s_abort, prm.wait_limit));
+    if (ok) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16* orow = prm.o + ((static_cast<long long>(b) * prm.Lq + qrow) * prm.Hq + h) * D;
@@ -402,7 +417,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
       if (qrow < prm.Lq && prm.lse != nullptr)
         prm.lse[(static_cast<long long>(b) * prm.Hq + h) * prm.Lq + qrow] =
             (m_used + log2f(l_run)) * 0.69314718055994531f;
-    } else if (ok) {
+    } else {
       fail(10);
     }
   }
@@ -445,6 +460,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
   // arithmetic cannot overflow).
   p.w0 = a.window_only ? std::min(a.w0, 1 << 30) : ((a.G == 1 || a.w0 >= a.Lk) ? (1 << 30) : a.w0);
   p.window_only = a.window_only ? 1 : 0;
+  p.wait_limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimit;
   p.G = a.G;
   p.npairs = (a.Lq + 2 * kBM - 1) / (2 * kBM);
   p.scale_log2 = a.scale_log2;

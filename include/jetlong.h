@@ -326,6 +326,24 @@ int jl_device_status(void* cuda_stream);
  */
 int jl_selftest_bounded_wait(long long limit_cycles, void* cuda_stream);
 
+/*
+ * Test support for the bounded waits of the prefill pipeline: exactly
+ * jl_bifocal_prefill (no k_rot_out, default softmax scale), except that every
+ * wait of the attention kernel's pipeline gives up after `limit_cycles`
+ * clock cycles (1 .. 4e9) instead of about 2 s.  With a small limit the
+ * waits run out: the CTAs record a status code, let their bulk copies and
+ * tensor-core work finish, free their tensor memory and return, so the next
+ * jl_device_status on the stream reports JL_ERR_TIMEOUT and the context stays
+ * usable; o and lse are then incomplete.  The paper has no counterpart.
+ */
+int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v,
+                                   void* o, float* lse,
+                                   int B, int L, int Hq, int Hkv, int d,
+                                   int w0, int w_pretrained, double rope_theta,
+                                   long long limit_cycles,
+                                   void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream);
+
 /* Message of the last error on this thread ("" if none). Never NULL. */
 const char* jl_last_error(void);
 
