@@ -434,23 +434,24 @@ def run_profile_prefill(args):
     import bifocal_rope_extension_causal_b300 as jl
     w = PREFILL
     L = int(args.profile_prefill)
+    wp = int(args.profile_wp) if args.profile_wp else w.w_pretrained
     dev = torch.device("cuda", 0)
     q, k, v = synth.prefill_inputs(L, w.Hq, w.Hkv, w.d, w.index)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    ws = jl.alloc_workspace(jl.prefill_workspace_size(1, L, w.Hq, w.Hkv, w.d, w.w_pretrained), dev)
+    ws = jl.alloc_workspace(jl.prefill_workspace_size(1, L, w.Hq, w.Hkv, w.d, wp), dev)
     for _ in range(args.warmup):
-        jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws)
+        jl.prefill(qd, kd, vd, w.w0, wp, w.theta, workspace=ws)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(args.steps):
-        jl.prefill(qd, kd, vd, w.w0, w.w_pretrained, w.theta, workspace=ws)
+        jl.prefill(qd, kd, vd, w.w0, wp, w.theta, workspace=ws)
     b.record()
     torch.cuda.synchronize()
     jl.device_status()
     ms = a.elapsed_time(b) / args.steps
     flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
-    print(json.dumps({"profile_prefill_L": L, "G": jl.group_size(L, w.w_pretrained), "ms": ms,
+    print(json.dumps({"profile_prefill_L": L, "w_pretrained": wp, "G": jl.group_size(L, wp), "ms": ms,
                       "tflops": flops / (ms * 1e-3) / 1e12}))
     return 0
 
@@ -657,6 +658,9 @@ def main():
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                     help="profiling mode: only the prefill of the 4x-extension head layout at "
                          "sequence length L (G from L), warm-up + steps calls; prints timings")
+    ap.add_argument("--profile-wp", type=int, default=0, metavar="W",
+                    help="with --profile-prefill: pretrained length W instead of the workload's "
+                         "(G = ceil(L / W); small L with G > 1 exercises the remote phase)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
     if args.impl == "reference":

@@ -170,6 +170,14 @@ int jl_bifocal_prefill_chunk(const void* q, const void* k, const void* v,
  * from B's, so its error grows where the local window holds most of the
  * aliased-rotation mass.  It scores the window pairs three times.
  *
+ * Fidelity: this A/B form does NOT always meet the acceptance bound of the
+ * routed prefill (O max-abs 2e-2 against the fp64 reference).  On random
+ * inputs the two forms agree to about 3e-3 (O) and 4e-6 (LSE), but where
+ * each query's own window dominates (queries close to their own keys) the
+ * measured O max-abs error of the three-pass form reached 2.7e-2, against
+ * 1.5e-2 for jl_bifocal_prefill on the same inputs.  Use jl_bifocal_prefill
+ * when the bound matters; this entry point exists for comparison.
+ *
  * Arguments, layouts and errors as jl_bifocal_prefill (no k_rot_out);
  * workspace >= jl_bifocal_prefill_three_pass_workspace_size(...) bytes, which
  * holds the rotated operands, oA, oC and the three log-sum-exps.

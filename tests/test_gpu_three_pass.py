@@ -85,8 +85,11 @@ def peaked_local_inputs(L, Hq, Hkv, d, seed, gain):
 
 # The three-pass merge combines three bf16-rounded outputs; where the window
 # dominates, w_A ~ w_B ~ w_C and den ~ w_A, so its O error is about three
-# times one pass's output rounding.  Its bound in that case is twice the
-# acceptance bound; the routed single pass meets the acceptance bounds.
+# times one pass's output rounding (2.7e-2 measured, against the 2e-2
+# acceptance bound that the routed single pass meets).  The A/B form is held
+# to twice the acceptance bound in that case, and the public header states
+# the measured figure: this is a documented limit of the A/B entry point,
+# not the acceptance bound of the prefill.
 THREE_PASS_CANCEL_O_MAX = 4e-2
 
 
