@@ -71,6 +71,7 @@ struct Cfg {
 
 struct TcParams {
   int B, Lq, q_base, Hq, Hkv, w0, G, npairs;
+  int pair_block;  // query-tile pairs per scheduling block (about one wave per KV head)
   int window_only;  // skip the remote phase (local views of the three-pass form)
   long long wait_limit;  // clock cycles a pipeline wait may take before the CTA gives up
   float scale_log2;
@@ -125,12 +126,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
   const uint32_t sRing = smem_base + 2 * kTileBytes;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BH = prm.B * prm.Hq;
+  // Grid order: blocks of pair_block query-tile pairs, longest rows first;
+  // within a block, batch, then KV head, then pair, then the query heads of
+  // the KV head.  A resident wave (about one CTA per SM) is then the query
+  // heads of one KV head over adjacent tile pairs, which walk the same K/V
+  // tiles at about the same time, so most K/V reads are served from L2.
+  const int gqh = prm.Hq / prm.Hkv;
   const int u = blockIdx.x;
-  const int pair = prm.npairs - 1 - u / BH;  // longest rows first
-  const int bh = u % BH;
-  const int b = bh / prm.Hq, h = bh % prm.Hq;
-  const int hk = h / (prm.Hq / prm.Hkv);
+  const int per_block = prm.pair_block * prm.B * prm.Hq;  // CTAs of a full block
+  const int blk = u / per_block, rin = u % per_block;
+  const int p_hi = prm.npairs - 1 - blk * prm.pair_block;  // longest pair of the block
+  const int nb = min(prm.pair_block, p_hi + 1);            // pairs in this block
+  const int hq_in = rin % gqh, pi = (rin / gqh) % nb, bk = rin / (gqh * nb);
+  const int b = bk / prm.Hkv, hk = bk % prm.Hkv;
+  const int pair = p_hi - pi;
+  const int h = hk * gqh + hq_in;
   const int row0 = pair * 2 * kBM;        // first query row of the CTA (local)
   const int q0 = prm.q_base + row0;       // its position
   const Plan plan = make_plan(q0, prm.q_base + prm.Lq, prm.w0, prm.window_only != 0);
@@ -463,6 +473,11 @@ cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
   p.wait_limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimit;
   p.G = a.G;
   p.npairs = (a.Lq + 2 * kBM - 1) / (2 * kBM);
+  {
+    int dev = 0, nsm = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    p.pair_block = std::max(1, std::min(p.npairs, nsm / (a.Hq / a.Hkv)));
+  }
   p.scale_log2 = a.scale_log2;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
