@@ -499,6 +499,63 @@ def run_profile_three_pass(args):
     return 0
 
 
+def run_profile_cta_pair(args):
+    """A/B of the two attention kernels on the 4x-extension shapes at sequence
+    length L (pretrained length from --profile-wp, else the workload's): the
+    default single-CTA kernel (jl_bifocal_attention) against the CTA-pair
+    kernel (jl_bifocal_attention_cta_pair), both after one jl_bifocal_rope
+    into the same workspace, interleaved per round; min over rounds."""
+    import ctypes
+    import torch
+    import bifocal_rope_extension_causal_b300 as jl
+    from bifocal_rope_extension_causal_b300 import _capi
+    w = PREFILL
+    L = int(args.profile_cta_pair)
+    wp = int(args.profile_wp) if args.profile_wp else w.w_pretrained
+    dev = torch.device("cuda", 0)
+    q, k, v = synth.prefill_inputs(L, w.Hq, w.Hkv, w.d, w.index)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    nbytes = jl.prefill_workspace_size(1, L, w.Hq, w.Hkv, w.d, wp)
+    ws = jl.alloc_workspace(nbytes, dev)
+    lib, P = _capi.load(), ctypes.c_void_p
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    _capi.check(lib.jl_bifocal_rope(P(qd.data_ptr()), P(kd.data_ptr()), 1, L, w.Hq, w.Hkv, w.d, wp, w.theta, None,
+                                    P(ws.data_ptr()), nbytes, stream))
+    outs = {n: (torch.empty_like(qd), torch.empty((1, w.Hq, L), dtype=torch.float32, device=dev))
+            for n in ("single_cta", "cta_pair")}
+    fns = {"single_cta": lib.jl_bifocal_attention, "cta_pair": lib.jl_bifocal_attention_cta_pair}
+
+    def run(name):
+        o, lse = outs[name]
+        _capi.check(fns[name](P(vd.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()), 1, L, w.Hq, w.Hkv, w.d, w.w0,
+                              wp, 0.0, P(ws.data_ptr()), nbytes, stream))
+
+    for _ in range(args.warmup):
+        for name in fns:
+            run(name)
+    torch.cuda.synchronize()
+    times = {n: [] for n in fns}
+    for _ in range(args.steps):
+        for name in fns:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run(name)
+            b.record()
+            torch.cuda.synchronize()
+            times[name].append(a.elapsed_time(b))
+    jl.device_status()
+    flops = 4.0 * w.d * (L * (L + 1) // 2) * w.Hq
+    res = {}
+    for name in fns:
+        ms = min(times[name])
+        res[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+    (o1, l1), (o2, l2) = outs["single_cta"], outs["cta_pair"]
+    print(json.dumps({"profile_cta_pair_L": L, "w_pretrained": wp, "G": jl.group_size(L, wp), **res,
+                      "o_maxabs_diff": float((o1.float() - o2.float()).abs().max()),
+                      "lse_maxabs_diff": float((l1 - l2).abs().max())}))
+    return 0
+
+
 def run_profile_decode(args):
     """Decode steps of the decode workload at one cache length, for ncu."""
     import torch
@@ -658,8 +715,11 @@ def main():
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                     help="profiling mode: only the prefill of the 4x-extension head layout at "
                          "sequence length L (G from L), warm-up + steps calls; prints timings")
+    ap.add_argument("--profile-cta-pair", type=int, default=0, metavar="L",
+                    help="profiling mode: A/B of the single-CTA and CTA-pair attention kernels on the "
+                         "4x-extension head layout at sequence length L; prints both timings")
     ap.add_argument("--profile-wp", type=int, default=0, metavar="W",
-                    help="with --profile-prefill: pretrained length W instead of the workload's "
+                    help="with --profile-prefill or --profile-cta-pair: pretrained length W instead of the workload's "
                          "(G = ceil(L / W); small L with G > 1 exercises the remote phase)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
@@ -667,6 +727,8 @@ def main():
         return run_reference(args)
     if args.profile_prefill:
         return run_profile_prefill(args)
+    if args.profile_cta_pair:
+        return run_profile_cta_pair(args)
     if args.profile_three_pass:
         return run_profile_three_pass(args)
     if args.profile_decode_varlen:

@@ -46,6 +46,12 @@ SIGNATURES = {
         _c.c_int, _c.c_int, _c.c_float,                    # w0, w_pretrained, softmax_scale
         _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
     ]),
+    "jl_bifocal_attention_cta_pair": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # v, o, lse
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,  # B, L, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_float,                    # w0, w_pretrained, softmax_scale
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_bifocal_prefill_chunk_workspace_size": (_c.c_size_t, [_c.c_int] * 7),
     "jl_bifocal_prefill_chunk": (_c.c_int, [
         _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k, v (chunk, raw)

@@ -180,10 +180,11 @@ int jl_bifocal_rope(const void* q, const void* k, int B, int L, int Hq, int Hkv,
 
 namespace {
 
-// jl_bifocal_attention with a given pipeline wait limit (0: the default).
+// jl_bifocal_attention with a given pipeline wait limit (0: the default) and
+// kernel (cta_pair: the CTA-pair kernel, head dim 128).
 int attention_call(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d, int w0,
                    int w_pretrained, float softmax_scale, const void* workspace, size_t workspace_bytes,
-                   long long wait_limit, void* cuda_stream) {
+                   long long wait_limit, bool cta_pair, void* cuda_stream) {
   if (!v || !o) return fail(JL_ERR_INVALID, "attention: null v/o pointer");
   int rc = check_prefill_shape("attention", B, L, Hq, Hkv, d, w0, w_pretrained);
   if (rc != JL_OK) return rc;
@@ -204,6 +205,7 @@ int attention_call(const void* v, void* o, float* lse, int B, int L, int Hq, int
   a.B = B; a.Lq = L; a.Lk = L; a.q_base = 0; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.w0 = w0; a.G = G;
   a.scale_log2 = resolve_scale(softmax_scale, d) * kLog2e;
   a.wait_limit = wait_limit;
+  a.cta_pair = cta_pair;
   const cudaError_t e = launch_prefill_attention(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention: kernel launch");
   return JL_OK;
@@ -218,7 +220,16 @@ int jl_bifocal_attention(const void* v, void* o, float* lse, int B, int L, int H
                          size_t workspace_bytes, void* cuda_stream) {
   t_err[0] = '\0';
   return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, softmax_scale, workspace, workspace_bytes,
-                        0, cuda_stream);
+                        0, false, cuda_stream);
+}
+
+int jl_bifocal_attention_cta_pair(const void* v, void* o, float* lse, int B, int L, int Hq, int Hkv, int d,
+                                  int w0, int w_pretrained, float softmax_scale, const void* workspace,
+                                  size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  if (d != 128) return fail(JL_ERR_UNSUPPORTED, "attention_cta_pair: head dim 128 only (d = %d)", d);
+  return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, softmax_scale, workspace, workspace_bytes,
+                        0, true, cuda_stream);
 }
 
 int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -233,7 +244,7 @@ int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v, 
                            workspace_bytes, cuda_stream);
   if (rc != JL_OK) return rc;
   return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, 0.f, workspace, workspace_bytes,
-                        limit_cycles, cuda_stream);
+                        limit_cycles, false, cuda_stream);
 }
 
 int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -85,8 +85,13 @@ struct PrefillArgs {
   // status code and skips its remaining work); 0 selects the default
   // (about 2 s).  Only the test-support entry point sets it.
   long long wait_limit = 0;
+  // Head dim 128 only: run on CTA pairs (prefill_pair.cu) instead of the
+  // single-CTA kernel; the A/B counterpart, slower on B300.
+  bool cta_pair = false;
 };
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+// Head dim 128 on CTA pairs (prefill_pair.cu); `status` is the device status word.
+cudaError_t launch_prefill_attention_pair(const PrefillArgs& a, int* status, cudaStream_t stream);
 
 // ---- Three-pass merge (three_pass.cu) ----------------------------------------
 // o = (wA oA + wB o - wC oC) / (wA + wB - wC), w_X = exp(lse_X - max(lse_A, lse_B)),

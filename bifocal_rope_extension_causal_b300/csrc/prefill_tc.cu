@@ -233,64 +233,70 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issue
-    if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false);
-      const uint32_t id_pv = idesc_bf16_f32(kBM, D, true);
-      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, prm.wait_limit);
-      if (!ok) fail(3);
-      auto wait_slot = [&](int idx) {
-        const int s = idx % kSlots;
-        if (!mbar_wait(bar(bars.full[s]), (idx / kSlots) & 1, &s_abort, prm.wait_limit)) { fail(4); return false; }
-        tc_fence_after();
-        return true;
-      };
-      auto pv = [&](int t, int vprev) {  // O_t += P_t V(vprev)
-        if (!mbar_wait(bar(bars.p_full[t]), vprev & 1, &s_abort, prm.wait_limit)) { fail(5); return false; }
-        tc_fence_after();
-        const uint32_t vs = sRing + ((2 * vprev + 1) % kSlots) * kTileBytes;
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                 desc_sw128(vs + kk * 2048, Cfg<D>::kVLbo, Cfg<D>::kVSbo),
-                 id_pv, (vprev > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(bars.pv_done[t]));
-        return true;
-      };
-      for (int v = 0; v < plan.nv && ok; ++v) {
-        if (v > 0 && !(ok = wait_slot(2 * (v - 1) + 1))) break;  // V of the previous visit
-        if (!(ok = wait_slot(2 * v))) break;                     // K of this visit
-        const uint32_t ks = sRing + ((2 * v) % kSlots) * kTileBytes;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (v > 0) {
-            if (!(ok = pv(t, v - 1))) break;
-            if (t == 1) mma_commit(bar(bars.empty[(2 * (v - 1) + 1) % kSlots]));
-          }
-          if (t == 0 && v == plan.nr && v > 0) {  // first local visit: Q_abs resident?
-            if (!(ok = mbar_wait(bar(bars.q_full), 1, &s_abort, prm.wait_limit))) { fail(6); break; }
-            tc_fence_after();
-          }
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + t * 128, desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
-                   desc_sw128(ks + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(bars.s_full[t]));
+    // The whole warp runs the loop, so the descriptors and addresses are
+    // warp-uniform (uniform registers); one elected lane issues each
+    // operation.  Wait outcomes are made warp-uniform.
+    const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false);
+    const uint32_t id_pv = idesc_bf16_f32(kBM, D, true);
+    const uint64_t qdesc[2] = {desc_sw128(sQ, 16, 1024), desc_sw128(sQ + kTileBytes, 16, 1024)};
+    auto wait = [&](uint32_t b, uint32_t parity, int code) {
+      const bool r = __all_sync(0xffffffffu, mbar_wait(b, parity, &s_abort, prm.wait_limit));
+      if (!r && lane == 0) fail(code);
+      return r;
+    };
+    auto wait_slot = [&](int idx) {
+      if (!wait(bar(bars.full[idx % kSlots]), (idx / kSlots) & 1, 4)) return false;
+      tc_fence_after();
+      return true;
+    };
+    auto pv = [&](int t, int vprev) {  // O_t += P_t V(vprev)
+      if (!wait(bar(bars.p_full[t]), vprev & 1, 5)) return false;
+      tc_fence_after();
+      const uint64_t vdesc = desc_sw128(sRing + ((2 * vprev + 1) % kSlots) * kTileBytes, Cfg<D>::kVLbo, Cfg<D>::kVSbo);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)  // 16 keys = 2048 bytes per step
+        mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vdesc + (kk * 2048 >> 4), id_pv,
+                     (vprev > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(bar(bars.pv_done[t]));
+      return true;
+    };
+    bool ok = wait(bar(bars.q_full), 0, 3);
+    for (int v = 0; v < plan.nv && ok; ++v) {
+      if (v > 0 && !(ok = wait_slot(2 * (v - 1) + 1))) break;  // V of the previous visit
+      if (!(ok = wait_slot(2 * v))) break;                     // K of this visit
+      // Descriptors advance by their start-address field (bytes >> 4).
+      const uint64_t kdesc = desc_sw128(sRing + ((2 * v) % kSlots) * kTileBytes, 16, 1024);
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (v > 0) {
+          if (!(ok = pv(t, v - 1))) break;
+          if (t == 1) mma_commit_elect(bar(bars.empty[(2 * (v - 1) + 1) % kSlots]));
         }
-        if (!ok) break;
-        mma_commit(bar(bars.empty[(2 * v) % kSlots]));
-        if (v == plan.nr - 1 && plan.nr < plan.nv) mma_commit(bar(bars.q_empty));
+        if (t == 0 && v == plan.nr && v > 0) {  // first local visit: Q_abs resident?
+          if (!(ok = wait(bar(bars.q_full), 1, 6))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss_elect(tmem + t * 128, qdesc[t] + off, kdesc + off, id_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(bar(bars.s_full[t]));
       }
-      if (ok) {
-        const int vl = plan.nv - 1;
-        ok = wait_slot(2 * vl + 1);
-        for (int t = 0; t < 2 && ok; ++t) ok = pv(t, vl);
-        if (ok) mma_commit(bar(bars.empty[(2 * vl + 1) % kSlots]));
-      }
-      // Drain: every MMA issued by this thread completes before TMEM is freed.
-      mma_commit(bar(bars.mma_final));
-      const volatile int never = 0;
-      if (!mbar_wait(bar(bars.mma_final), 0, &never, kWaitLimit)) atomicCAS(prm.status, 0, 7);
+      if (!ok) break;
+      mma_commit_elect(bar(bars.empty[(2 * v) % kSlots]));
+      if (v == plan.nr - 1 && plan.nr < plan.nv) mma_commit_elect(bar(bars.q_empty));
     }
-    __syncwarp();
+    if (ok) {
+      const int vl = plan.nv - 1;
+      ok = wait_slot(2 * vl + 1);
+      for (int t = 0; t < 2 && ok; ++t) ok = pv(t, vl);
+      if (ok) mma_commit_elect(bar(bars.empty[(2 * vl + 1) % kSlots]));
+    }
+    // Drain: every MMA issued by this warp completes before TMEM is freed.
+    mma_commit_elect(bar(bars.mma_final));
+    const volatile int never = 0;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.mma_final), 0, &never, kWaitLimit)) && lane == 0)
+      atomicCAS(prm.status, 0, 7);
   } else {
     // ------------------------------------------------------------ softmax warps
     const int t = warp >> 2;           // query tile
@@ -497,6 +503,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int* status, cudaStream_t stream) {
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream) {
   int* status = device_status_ptr();
   if (status == nullptr) return cudaErrorInvalidSymbol;
+  if (a.d == 128 && a.cta_pair) return launch_prefill_attention_pair(a, status, stream);
   if (a.d == 128) return launch_tc<128>(a, status, stream);
   if (a.d == 64) return launch_tc<64>(a, status, stream);
   return cudaErrorInvalidValue;

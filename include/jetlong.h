@@ -121,6 +121,22 @@ int jl_bifocal_attention(const void* v, void* o, float* lse,
                          void* cuda_stream);
 
 /*
+ * The same computation as jl_bifocal_attention (same arguments, workspace,
+ * results and error behaviour) on a second kernel design, kept as its A/B
+ * counterpart: each tensor-core operation is shared by a cluster of two CTAs
+ * (tcgen05 cta_group::2, M = 256), so that each CTA holds one 128-row query
+ * tile with a double-buffered score tile.  Head dim 128 only
+ * (JL_ERR_UNSUPPORTED otherwise).  Outputs are within the same bounds of the
+ * oracle; on B300 it is slower than jl_bifocal_attention (paper digest page,
+ * "Method", Eq. 1 for what it computes).
+ */
+int jl_bifocal_attention_cta_pair(const void* v, void* o, float* lse,
+                                  int B, int L, int Hq, int Hkv, int d,
+                                  int w0, int w_pretrained, float softmax_scale,
+                                  const void* workspace, size_t workspace_bytes,
+                                  void* cuda_stream);
+
+/*
  * Chunked prefill against an absolute-position KV cache: the prompt arrives
  * in chunks, and each chunk attends to everything before it through the
  * cache that earlier calls filled (this entry point, jl_bifocal_prefill's

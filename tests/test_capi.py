@@ -99,6 +99,22 @@ def test_prefill_argument_checks(lib, kw, code):
     assert lib.jl_last_error().decode()
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), _capi.JL_ERR_UNSUPPORTED),
+    (dict(v=None), _capi.JL_ERR_INVALID),
+    (dict(Hq=3, Hkv=2), _capi.JL_ERR_INVALID),
+    (dict(wsb=16), _capi.JL_ERR_WORKSPACE),
+])
+def test_cta_pair_attention_argument_checks(lib, kw, code):
+    """The CTA-pair kernel takes head dim 128 only and the attention checks."""
+    a = dict(v=1 << 20, o=1 << 20, lse=None, B=1, L=128, Hq=2, Hkv=1, d=128, w0=16, wp=64, scale=0.0,
+             ws=1 << 20, wsb=1 << 30, stream=None)
+    a.update(kw)
+    assert lib.jl_bifocal_attention_cta_pair(a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"], a["Hkv"], a["d"],
+                                             a["w0"], a["wp"], a["scale"], a["ws"], a["wsb"], a["stream"]) == code
+    assert lib.jl_last_error().decode()
+
+
 def _three_pass_args(**kw):
     a = dict(q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, lse=None, B=1, L=128, Hq=2, Hkv=1, d=128,
              w0=16, wp=64, theta=1e4, scale=0.0, ws=1 << 20, wsb=1 << 30, stream=None)
