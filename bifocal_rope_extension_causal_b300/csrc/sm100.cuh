@@ -37,14 +37,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One test of the phase; while it is incomplete the thread may be suspended
+// for up to `hint_ns` and is resumed as soon as the phase completes, so a
+// waiting thread neither spins nor takes issue slots from the others.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -54,9 +57,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // that a broken pipeline ends the kernel instead of hanging the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // Suspension slices of at most 1 ms, and short enough (about half the
+  // limit in ns at ~2 cycles per ns) that a small limit still runs out.
+  const uint32_t hint = static_cast<uint32_t>(limit >= 2000000 ? 1000000 : limit / 2);
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait(bar, parity, hint)) {
     if (*abort != 0 || clock64() - t0 > limit) return false;
   }
   return true;
