@@ -366,26 +366,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_consta
       const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_exp, -m_exp);
       float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
-      uint32_t pk0[32], pk1[32];
+      // P columns 0..63 (bf16 pairs) over S columns already read, stored 16
+      // columns at a time so that few packed registers are live next to S.
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float2 a = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
-        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-        pk0[i] = pack_bf16x2(e.x, e.y);
-      }
-      tmem_st32(tS + 0, pk0);  // P columns 0..31 over S columns already read
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float2 a = __ffma2_rn(make_float2(s[64 + 2 * i], s[64 + 2 * i + 1]), sc2, nm2);
-        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-        pk1[i] = pack_bf16x2(e.x, e.y);
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * q4 + 2 * i;
+          const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+          const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+          pk[i] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st16(tS + 16 * q4, pk);
       }
       const float2 t2 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       const float rowsum = t2.x + t2.y;
       l_run = l_run * factor + rowsum;
-      tmem_st32(tS + 32, pk1);
       // Rescale O_t in tensor memory when any row of this warp raised its max.
       if (v > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.pv_done[t]), (v - 1) & 1, &s_abort, prm.wait_limit));
