@@ -348,41 +348,38 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_qa, const __grid_cons
       visit_of(plan, v, j, remote);
       const int kh = j * kBN + hf * 64;  // first key of this warp's columns
       const int x = v & 1;
-      bool wok = ok && __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[x]), (v >> 1) & 1, &s_abort, prm.wait_limit));
+      const bool wok = ok && __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[x]), (v >> 1) & 1, &s_abort, prm.wait_limit));
+      // The scores are loaded even when the wait gave up (the values are
+      // then unused: both warps of the row leave at the exchange below), so
+      // that they have a single definition.
+      tc_fence_after();
+      uint32_t a0[32], a1[32];
+      tmem_ld32(tmem + lane_base + x * 128 + hf * 64, a0);
+      tmem_ld32(tmem + lane_base + x * 128 + hf * 64 + 32, a1);
+      tmem_ld_wait(a0);
+      tmem_ld_wait(a1);
       float s[64];
-      float mx = -INFINITY;
-      if (wok) {
-        tc_fence_after();
-        uint32_t a0[32], a1[32];
-        tmem_ld32(tmem + lane_base + x * 128 + hf * 64, a0);
-        tmem_ld32(tmem + lane_base + x * 128 + hf * 64 + 32, a1);
-        tmem_ld_wait(a0);
-        tmem_ld_wait(a1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(a0[i]);
-          s[32 + i] = __uint_as_float(a1[i]);
-        }
-        const bool need_mask = remote ? remote_visit_needs_mask(q0t, kBM, kh, 64, w0)
-                                      : local_visit_needs_mask(q0t, kBM, kh, 64, w0);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (!visit_keeps(remote, q, kh + c, w0)) s[c] = -INFINITY;
-        }
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = s[k];
-#pragma unroll
-        for (int c = 8; c < 64; c += 8)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[c + k]);
-        mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+      for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(a0[i]);
+        s[32 + i] = __uint_as_float(a1[i]);
       }
+      const bool need_mask = remote ? remote_visit_needs_mask(q0t, kBM, kh, 64, w0)
+                                    : local_visit_needs_mask(q0t, kBM, kh, 64, w0);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!visit_keeps(remote, q, kh + c, w0)) s[c] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < 64; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[c + k]);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // Row max over both halves.
       s_xmax[x][warp][lane] = mx;
       s_xok[x][warp][lane] = wok ? 1 : 0;
