@@ -112,6 +112,14 @@ SIGNATURES = {
         _c.c_longlong,                                     # limit_cycles
         _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
     ]),
+    "jl_selftest_prefill_pair_wait_limit": (_c.c_int, [
+        _c.c_void_p, _c.c_void_p, _c.c_void_p,            # q, k, v
+        _c.c_void_p, _c.c_void_p,                          # o, lse
+        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,  # B, L, Hq, Hkv, d
+        _c.c_int, _c.c_int, _c.c_double,                   # w0, w_pretrained, theta
+        _c.c_longlong,                                     # limit_cycles
+        _c.c_void_p, _c.c_size_t, _c.c_void_p,             # workspace, bytes, stream
+    ]),
     "jl_last_error": (_c.c_char_p, []),
 }
 

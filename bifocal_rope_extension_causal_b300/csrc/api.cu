@@ -232,19 +232,44 @@ int jl_bifocal_attention_cta_pair(const void* v, void* o, float* lse, int B, int
                         0, true, cuda_stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+int selftest_wait_limit(const void* q, const void* k, const void* v, void* o, float* lse, int B, int L, int Hq,
+                        int Hkv, int d, int w0, int w_pretrained, double rope_theta, long long limit_cycles,
+                        void* workspace, size_t workspace_bytes, bool cta_pair, void* cuda_stream) {
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL)
+    return fail(JL_ERR_INVALID, "selftest: limit_cycles must be in [1, 4e9]");
+  if (!q || !k || !v || !o) return fail(JL_ERR_INVALID, "selftest: null q/k/v/o pointer");
+  if (cta_pair && d != 128) return fail(JL_ERR_UNSUPPORTED, "selftest: the CTA-pair kernel takes head dim 128 only");
+  int rc = jl_bifocal_rope(q, k, B, L, Hq, Hkv, d, w_pretrained, rope_theta, nullptr, workspace,
+                           workspace_bytes, cuda_stream);
+  if (rc != JL_OK) return rc;
+  return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, 0.f, workspace, workspace_bytes,
+                        limit_cycles, cta_pair, cuda_stream);
+}
+
+}  // namespace
+
+extern "C" {
+
 int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                                    int L, int Hq, int Hkv, int d, int w0, int w_pretrained, double rope_theta,
                                    long long limit_cycles, void* workspace, size_t workspace_bytes,
                                    void* cuda_stream) {
   t_err[0] = '\0';
-  if (limit_cycles < 1 || limit_cycles > 4000000000LL)
-    return fail(JL_ERR_INVALID, "selftest: limit_cycles must be in [1, 4e9]");
-  if (!q || !k || !v || !o) return fail(JL_ERR_INVALID, "selftest: null q/k/v/o pointer");
-  int rc = jl_bifocal_rope(q, k, B, L, Hq, Hkv, d, w_pretrained, rope_theta, nullptr, workspace,
-                           workspace_bytes, cuda_stream);
-  if (rc != JL_OK) return rc;
-  return attention_call(v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, 0.f, workspace, workspace_bytes,
-                        limit_cycles, false, cuda_stream);
+  return selftest_wait_limit(q, k, v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, rope_theta, limit_cycles,
+                             workspace, workspace_bytes, false, cuda_stream);
+}
+
+int jl_selftest_prefill_pair_wait_limit(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                        int L, int Hq, int Hkv, int d, int w0, int w_pretrained,
+                                        double rope_theta, long long limit_cycles, void* workspace,
+                                        size_t workspace_bytes, void* cuda_stream) {
+  t_err[0] = '\0';
+  return selftest_wait_limit(q, k, v, o, lse, B, L, Hq, Hkv, d, w0, w_pretrained, rope_theta, limit_cycles,
+                             workspace, workspace_bytes, true, cuda_stream);
 }
 
 int jl_bifocal_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -368,6 +368,21 @@ int jl_selftest_prefill_wait_limit(const void* q, const void* k, const void* v,
                                    void* workspace, size_t workspace_bytes,
                                    void* cuda_stream);
 
+/*
+ * The same test support for the CTA-pair attention kernel
+ * (jl_bifocal_attention_cta_pair, d = 128 only; JL_ERR_UNSUPPORTED
+ * otherwise): with a small limit both CTAs of a pair give up, tell each
+ * other, drain their copies and tensor-core work, meet at the cluster
+ * barrier, free the pair's tensor memory and return.
+ */
+int jl_selftest_prefill_pair_wait_limit(const void* q, const void* k, const void* v,
+                                        void* o, float* lse,
+                                        int B, int L, int Hq, int Hkv, int d,
+                                        int w0, int w_pretrained, double rope_theta,
+                                        long long limit_cycles,
+                                        void* workspace, size_t workspace_bytes,
+                                        void* cuda_stream);
+
 /* Message of the last error on this thread ("" if none). Never NULL. */
 const char* jl_last_error(void);
 

@@ -37,8 +37,9 @@ def test_selftest_argument_check():
     assert _capi.load().jl_selftest_bounded_wait(0, None) == _capi.JL_ERR_INVALID
 
 
+@pytest.mark.parametrize("kernel", ["single_cta", "cta_pair"])
 @pytest.mark.parametrize("limit", [1, 300])
-def test_prefill_pipeline_timeout_is_reported_and_context_survives(limit):
+def test_prefill_pipeline_timeout_is_reported_and_context_survives(limit, kernel):
     """The real attention pipeline with a wait limit small enough to run out:
     its CTAs give up, drain their bulk copies and tensor-core work, free
     their tensor memory and return; jl_device_status reports the timeout and
@@ -63,13 +64,17 @@ def test_prefill_pipeline_timeout_is_reported_and_context_survives(limit):
     nbytes = jl.prefill_workspace_size(1, L, Hq, Hkv, d, wp)
     ws = jl.alloc_workspace(nbytes, qd.device)
     assert lib.jl_device_status(stream) == _capi.JL_OK
-    _capi.check(lib.jl_selftest_prefill_wait_limit(P(qd.data_ptr()), P(kd.data_ptr()), P(vd.data_ptr()),
-                                                   P(o.data_ptr()), P(lse.data_ptr()), 1, L, Hq, Hkv, d, w0, wp,
-                                                   theta, limit, P(ws.data_ptr()), nbytes, stream))
+    selftest = (lib.jl_selftest_prefill_wait_limit if kernel == "single_cta"
+                else lib.jl_selftest_prefill_pair_wait_limit)
+    _capi.check(selftest(P(qd.data_ptr()), P(kd.data_ptr()), P(vd.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()),
+                         1, L, Hq, Hkv, d, w0, wp, theta, limit, P(ws.data_ptr()), nbytes, stream))
     assert lib.jl_device_status(stream) == _capi.JL_ERR_TIMEOUT
     assert b"bounded device wait" in lib.jl_last_error()
     assert lib.jl_device_status(stream) == _capi.JL_OK  # read-and-clear
     o2, l2 = jl.prefill(qd, kd, vd, w0, wp, theta, workspace=ws)
+    if kernel == "cta_pair":  # the same kernel again, without the limit
+        _capi.check(lib.jl_bifocal_attention_cta_pair(P(vd.data_ptr()), P(o2.data_ptr()), P(l2.data_ptr()), 1, L,
+                                                      Hq, Hkv, d, w0, wp, 0.0, P(ws.data_ptr()), nbytes, stream))
     jl.device_status()
     o_ref, l_ref = oracle.bifocal_prefill(q.float().numpy(), k.float().numpy(), v.float().numpy(), w0, wp, theta,
                                           round_rotated_qk=True)
@@ -83,3 +88,6 @@ def test_prefill_selftest_argument_check():
     rc = lib.jl_selftest_prefill_wait_limit(1 << 20, 1 << 20, 1 << 20, 1 << 20, None, 1, 64, 2, 1, 128, 4, 16,
                                             1e4, 0, 1 << 20, 1 << 30, None)
     assert rc == _capi.JL_ERR_INVALID
+    rc = lib.jl_selftest_prefill_pair_wait_limit(1 << 20, 1 << 20, 1 << 20, 1 << 20, None, 1, 64, 2, 1, 64, 4, 16,
+                                                 1e4, 100, 1 << 20, 1 << 30, None)
+    assert rc == _capi.JL_ERR_UNSUPPORTED
