@@ -81,38 +81,40 @@ def test_mid_sizes(jl, L, Hq, Hkv, d, wp, w0):
     full_check(jl, L, Hq, Hkv, d, wp, w0, 1e6, seed=L + w0)
 
 
-@pytest.mark.parametrize("L,Hq,Hkv,wp,w0", [
-    (65, 4, 1, 16, 0),         # one row past a tile, all remote but the diagonal
-    (129, 8, 2, 40, 7),        # G = 4, ragged, three tiles
-    (512, 4, 2, 128, 64),      # tile-aligned straddles
-    (3000, 4, 1, 800, 0),      # w0 = 0 over many tiles, G = 4
-    (2304, 8, 8, 300, 2303),   # every pair local at G = 8
+@pytest.mark.parametrize("L,Hq,Hkv,wp,w0,B", [
+    (65, 4, 1, 16, 0, 1),         # one row past a tile, all remote but the diagonal
+    (129, 8, 2, 40, 7, 1),        # G = 4, ragged, three tiles
+    (512, 4, 2, 128, 64, 1),      # tile-aligned straddles
+    (3000, 4, 1, 800, 0, 1),      # w0 = 0 over many tiles, G = 4
+    (2304, 8, 8, 300, 2303, 1),   # every pair local at G = 8
+    (1000, 16, 2, 300, 100, 1),   # GQA group 8, G = 4
+    (300, 4, 2, 100, 30, 2),      # batch of two, G = 3
 ])
-def test_cta_pair_kernel_matches_oracle(jl, L, Hq, Hkv, wp, w0):
+def test_cta_pair_kernel_matches_oracle(jl, L, Hq, Hkv, wp, w0, B):
     """The CTA-pair attention kernel (the A/B counterpart of the default
     kernel, head dim 128) after jl_bifocal_rope, against the oracle."""
     import ctypes
     import torch
     from bifocal_rope_extension_causal_b300 import _capi
     d, theta = 128, 1e6
-    q, k, v = synth.prefill_inputs(L, Hq, Hkv, d, L + w0)
+    q, k, v = synth.prefill_inputs(L, Hq, Hkv, d, L + w0, B=B)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.empty_like(qd)
-    lse = torch.empty((1, Hq, L), dtype=torch.float32, device="cuda")
-    nbytes = jl.prefill_workspace_size(1, L, Hq, Hkv, d, wp)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device="cuda")
+    nbytes = jl.prefill_workspace_size(B, L, Hq, Hkv, d, wp)
     ws = jl.alloc_workspace(nbytes, qd.device)
     lib, P = _capi.load(), ctypes.c_void_p
     stream = P(torch.cuda.current_stream().cuda_stream)
-    _capi.check(lib.jl_bifocal_rope(P(qd.data_ptr()), P(kd.data_ptr()), 1, L, Hq, Hkv, d, wp, theta, None,
+    _capi.check(lib.jl_bifocal_rope(P(qd.data_ptr()), P(kd.data_ptr()), B, L, Hq, Hkv, d, wp, theta, None,
                                     P(ws.data_ptr()), nbytes, stream))
-    _capi.check(lib.jl_bifocal_attention_cta_pair(P(vd.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()), 1, L, Hq,
+    _capi.check(lib.jl_bifocal_attention_cta_pair(P(vd.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()), B, L, Hq,
                                                   Hkv, d, w0, wp, 0.0, P(ws.data_ptr()), nbytes, stream))
     jl.device_status()
     qn, kn, vn = (x.float().numpy() for x in (q, k, v))
     o_r, l_r = oracle.bifocal_prefill(qn, kn, vn, w0, wp, theta, round_rotated_qk=True)
     o_p, _ = oracle.bifocal_prefill(qn, kn, vn, w0, wp, theta)
     og, lg = to_np(o), to_np(lse)
-    tag = f"cta pair L={L} Hq={Hq} Hkv={Hkv} wp={wp} w0={w0}"
+    tag = f"cta pair L={L} Hq={Hq} Hkv={Hkv} wp={wp} w0={w0} B={B}"
     assert_close(og, lg, o_r, l_r, tag + " (rounded oracle)")
     err = np.abs(og - o_p)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3, tag + " (plain oracle)"
