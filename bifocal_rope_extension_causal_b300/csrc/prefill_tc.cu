@@ -20,7 +20,8 @@
 // Roles (10 warps):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
-//   warp  8    tensor-core issue (one thread) and TMEM allocation
+//   warp  8    tensor-core issue (the whole warp runs the loop, one elected
+//              lane issues each MMA and commit) and TMEM allocation
 //   warp  9    TMA producer (one thread)
 // Tensor memory (512 columns): S_0, S_1 (fp32 scores, 128 columns each),
 // O_0, O_1 (fp32 outputs); P_t (bf16 probabilities) overwrites the first 64
@@ -31,8 +32,9 @@
 // Softmax: base-2 exponentials with scale * log2(e) folded in; the running
 // max is raised only when it grows by more than 8 (log2 units), so O is
 // rescaled in tensor memory rarely.  The row log-sum-exp is exported in
-// natural log.  Every barrier wait is bounded: on expiry the CTA records a
-// status code, drains its tensor-core work and exits.
+// natural log.  Every barrier wait is bounded (and suspends the thread rather
+// than spinning): on expiry the CTA records a status code, drains its bulk
+// copies and tensor-core work and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
