@@ -252,6 +252,11 @@ decode_partial_kernel(DecodeKParams p) {
   // Let the merge kernel (a programmatic dependent) launch early; it waits
   // for this grid's completion before reading the partials.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // This grid is itself a programmatic dependent of the preceding work on
+  // the stream (which may produce q or the cache, or still read the
+  // partials): its CTAs may be scheduled while that work finishes, and wait
+  // for it here, before touching any memory.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -771,6 +776,10 @@ decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
   constexpr int kV = D / 32;
   __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
   __shared__ __align__(16) float s_acc[kMergeWarps][D];
+  // The next grid on the stream may be scheduled now (a programmatic
+  // dependent such as the next decode's partial kernel waits for this grid
+  // before touching memory).
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // The partials are written by the preceding grid.
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -862,8 +871,20 @@ cudaError_t launch_partial(const dim3& grid, int warps, size_t smem, const Decod
   cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<D, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  decode_partial_kernel<D, GQ><<<grid, 32 * warps, smem, stream>>>(p);
-  return cudaGetLastError();
+  // A programmatic dependent of the preceding work on the stream (the kernel
+  // waits for it before touching memory), so that its launch overlaps that
+  // work's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(32 * warps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_partial_kernel<D, GQ>, p);
 }
 
 }  // namespace
